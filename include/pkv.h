@@ -1,0 +1,165 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged KV-cache write and PagedAttention on one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   [book]   "Implémentation du cœur du moteur d'inférence haute performance
+ *            vLLM" (AiReadCodeBooks); ch. 5 "slot_mapping et la block table",
+ *            ch. 6 "Transformation de la disposition mémoire du KV cache",
+ *            "Structure des métadonnées", "Flux des paramètres du chemin
+ *            non-cascadé", "Branche de masque", "Écriture du KV cache",
+ *            "build() étape par étape".
+ *   [gpuhub] "Khám phá vLLM: Giải phẫu hệ thống suy luận LLM thông lượng cao";
+ *            note under "KV cache manager" (block bytes), "allocate_slots"
+ *            step 1 (ceil(n/16) blocks), "Chạy forward pass" (flattened batch).
+ *
+ * Conventions shared by every call
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, on the
+ *     current CUDA device, 16-byte aligned, densely packed (row-major, no
+ *     padding) in the layout stated at the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work: they never allocate device memory,
+ *     never synchronise and never copy device data to the host, so they may be
+ *     captured into a CUDA graph.
+ *   - A call returns PKV_OK or a negative PKV_E_* for a host-side argument
+ *     error, in which case nothing was enqueued.  PKV_E_CUDA means a launch
+ *     failed; cudaGetLastError() holds the reason.
+ *   - Errors that depend on device data (a slot past the pool, a block id
+ *     outside [0, num_blocks), a context length outside
+ *     [1, block_table_stride * block_size], more queries than keys, a
+ *     "decode" sequence with a query length other than 1) never trap: the
+ *     offending item is skipped and a bit is OR-ed into a per-device error
+ *     word that pkv_get_error() returns.  Output rows of a sequence with a
+ *     metadata error are zero; with a bad block id they are unspecified.
+ *     Every other sequence is unaffected.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values) -------------------------------------- */
+#define PKV_OK 0
+#define PKV_E_NULL (-1)        /* a required pointer is NULL                     */
+#define PKV_E_DTYPE (-2)       /* dtype not PKV_F32 / PKV_BF16                   */
+#define PKV_E_SHAPE (-3)       /* unsupported head_size / block_size, or a size  */
+                               /* is negative or too large                       */
+#define PKV_E_GQA (-4)         /* num_q_heads not a multiple of num_kv_heads     */
+#define PKV_E_WORKSPACE (-5)   /* workspace smaller than pkv_attention_workspace_size */
+#define PKV_E_ALIGN (-6)       /* a pointer is not 16-byte aligned               */
+#define PKV_E_CUDA (-7)        /* a kernel launch or driver call failed          */
+#define PKV_E_META (-8)        /* inconsistent pkv_attn_meta fields              */
+
+/* ---- device error-word bits (see pkv_get_error) ------------------------- */
+#define PKV_ERR_SLOT (1 << 0)        /* pkv_write: slot >= num_blocks*block_size  */
+#define PKV_ERR_BLOCK_ID (1 << 1)    /* block id outside [0, num_blocks)         */
+#define PKV_ERR_CONTEXT_LEN (1 << 2) /* context_lens[s] < 1 with queries, or     */
+                                     /* > block_table_stride * block_size        */
+#define PKV_ERR_QUERY_LEN (1 << 3)   /* query length < 0 or > context_lens[s]    */
+#define PKV_ERR_DECODE_QLEN (1 << 4) /* a sequence below num_decode_seqs whose   */
+                                     /* query length is not 1                    */
+#define PKV_ERR_TIMEOUT (1 << 5)     /* an on-chip wait gave up (bounded spin)   */
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Shape of the paged KV cache ([book] ch. 6 "Transformation de la disposition
+ * mémoire du KV cache": separate K and V caches, each
+ * [num_blocks, block_size, num_kv_heads, head_size]).  One block of both
+ * caches takes 2 * block_size * num_kv_heads * head_size * dtype_bytes bytes
+ * ([gpuhub] note under "KV cache manager").
+ * Supported: block_size 16, head_size 64 or 128, dtype PKV_BF16 or PKV_F32. */
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_size;
+  int32_t dtype; /* pkv_dtype */
+} pkv_cache_desc;
+
+/* Host-side description of one attention batch ([book] ch. 6 "Structure des
+ * métadonnées"): the batch is flattened into num_tokens query rows
+ * ([gpuhub] "Chạy forward pass"), sequence s owning rows
+ * query_start_loc[s] .. query_start_loc[s+1]-1. */
+typedef struct {
+  int32_t num_seqs;           /* S                                              */
+  int32_t num_tokens;         /* T = query_start_loc[S] (rows of q and out)     */
+  int32_t num_q_heads;        /* Hq, a multiple of num_kv_heads (GQA)           */
+  int32_t block_table_stride; /* int32 entries per block_tables row (>= 1)      */
+  int32_t max_query_len;      /* >= every query length; 1 means pure decode     */
+  int32_t max_context_len;    /* >= every context_lens[s]; sizes split-K        */
+  int32_t num_decode_seqs;    /* sequences 0..n-1 have query length 1 (the      */
+                              /* decode run of a mixed batch); -1 = unknown     */
+  int32_t kv_split_tokens;    /* split-K chunk in keys for decode: 0 = choose   */
+                              /* automatically, else a multiple of 64 in        */
+                              /* [64, 2048]                                     */
+} pkv_attn_meta;
+
+/* KV-cache write ([book] ch. 6 "Écriture du KV cache"; ch. 5 on the -1 padding
+ * of slot_mapping): for every token t < num_tokens with slot =
+ * slot_mapping[t] >= 0, copies k[t] and v[t] (num_kv_heads * head_size
+ * elements each, bit for bit) into row `slot` of the caches, i.e. block
+ * slot / block_size, offset slot % block_size.  Slots < 0 are padding and are
+ * skipped.  A slot >= num_blocks * block_size is skipped and sets
+ * PKV_ERR_SLOT.  Two tokens with the same slot: the row written is one of
+ * the two (unspecified which).
+ *   k, v          [num_tokens, num_kv_heads, head_size], cache dtype
+ *   slot_mapping  int64 [num_tokens]
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_size]
+ * num_tokens == 0 is a no-op. */
+int pkv_write(const void *k, const void *v, const int64_t *slot_mapping,
+              int32_t num_tokens, void *k_cache, void *v_cache,
+              const pkv_cache_desc *cache, void *stream);
+
+/* Bytes of scratch workspace pkv_attention needs for this batch shape (the
+ * split buffer of [book] ch. 6 "build() étape par étape", fourth step: one
+ * fp32 partial output and one log-sum-exp per split, head and decode
+ * sequence).  0 when no split is needed.  Returns (size_t)-1 for an invalid
+ * description. */
+size_t pkv_attention_workspace_size(const pkv_cache_desc *cache,
+                                    const pkv_attn_meta *meta);
+
+/* PagedAttention ([book] ch. 6 "Flux des paramètres du chemin non-cascadé":
+ * cu_seqlens_q = query_start_loc, seqused_k = seq_lens; "Branche de masque").
+ * For each sequence s with L = context_lens[s] keys (history plus this step's
+ * new tokens, which pkv_write must already have stored) and q_s query rows,
+ * query row j sits at absolute position L - q_s + j and attends the keys
+ * p <= L - q_s + j; key p is read from block block_tables[s][p / block_size],
+ * offset p % block_size.  Query head hq uses kv head hq / (num_q_heads /
+ * num_kv_heads).  out[t][hq] = softmax(scale * q[t][hq] . K^T) V, accumulated
+ * in fp32 and rounded to the cache dtype (round to nearest even).
+ *   out, q            [num_tokens, num_q_heads, head_size], cache dtype
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_size]
+ *   block_tables      int32 [num_seqs, block_table_stride]; entries past
+ *                     ceil(L / block_size) are never read
+ *   context_lens      int32 [num_seqs]
+ *   query_start_loc   int32 [num_seqs + 1], non-decreasing, [0] = 0
+ *   workspace         device scratch of at least
+ *                     pkv_attention_workspace_size() bytes (may be NULL when
+ *                     that is 0); its contents need no initialisation.
+ * A sequence with q_s = 0 produces nothing.  Rows of out that belong to no
+ * sequence are not written. */
+int pkv_attention(void *out, const void *q, const void *k_cache,
+                  const void *v_cache, const int32_t *block_tables,
+                  const int32_t *context_lens, const int32_t *query_start_loc,
+                  float scale, const pkv_cache_desc *cache,
+                  const pkv_attn_meta *meta, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/* Reads (and, if clear != 0, resets) the current device's error word: the OR
+ * of PKV_ERR_* bits raised by kernels since the last clear.  SYNCHRONISES the
+ * device first.  Returns PKV_OK or PKV_E_CUDA. */
+int pkv_get_error(int32_t *error_bits, int clear);
+
+/* Static, human-readable text for a status code. */
+const char *pkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

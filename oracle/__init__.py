@@ -1,0 +1,207 @@
+"""CPU oracle for the paged KV-cache write and PagedAttention (fp64).
+
+TEST INFRASTRUCTURE ONLY.  The product path never imports, links or calls
+anything in this package: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` do.  It shares no code with the CUDA library
+in ``paged_kv_cache_43_gb300``; the two meet only through the seeded inputs of
+``paged_kv_cache_43_gb300.workloads``.
+
+Two independent implementations live here:
+
+* ``pkv_oracle.c`` (loaded through ctypes): walks each sequence's block table
+  key by key and accumulates in fp64, OpenMP-parallel over (row, head).
+* ``brute.py``: numpy, densifies each sequence's keys first and applies a
+  plain softmax; for tiny inputs only.
+
+Sources are the pages "Implémentation du cœur du moteur d'inférence haute
+performance vLLM" (AiReadCodeBooks), ch. 5 and ch. 6, and "Khám phá vLLM: Giải
+phẫu hệ thống suy luận LLM thông lượng cao" (KV cache manager note,
+allocate_slots); each function cites its section.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+
+
+class OrcProblem(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p),
+        ("v_cache", ctypes.c_void_p),
+        ("block_tables", ctypes.c_void_p),
+        ("context_lens", ctypes.c_void_p),
+        ("query_start_loc", ctypes.c_void_p),
+        ("bt_stride", ctypes.c_int64),
+        ("num_seqs", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_size", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pkv_oracle.c`` into ``_build/liboracle.so`` (gcc -O2, OpenMP,
+    no fast-math).  Returns the library path."""
+    with _lock:
+        if (not force and os.path.exists(_LIB_PATH)
+                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            return _LIB_PATH
+        os.makedirs(_OUT_DIR, exist_ok=True)
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+               "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.orc_write.restype = ctypes.c_int64
+        lib.orc_write.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_int32]
+        lib.orc_row_state.restype = ctypes.c_int
+        lib.orc_row_state.argtypes = [ctypes.POINTER(OrcProblem), ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                      ctypes.c_int64, ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
+        lib.orc_merge.restype = None
+        lib.orc_merge.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+        lib.orc_attention.restype = ctypes.c_int32
+        lib.orc_attention.argtypes = [ctypes.POINTER(OrcProblem), ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_int32]
+        lib.orc_max_threads.restype = ctypes.c_int32
+        lib.orc_max_threads.argtypes = []
+        _lib = lib
+    return _lib
+
+
+def _raw(a: np.ndarray) -> np.ndarray:
+    """A C-contiguous numpy array (bit patterns untouched)."""
+    return np.ascontiguousarray(a)
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def dtype_code(arr: np.ndarray) -> int:
+    """Storage code of a cache/query array: float32 -> F32, uint16 (bf16 bit
+    patterns) -> BF16."""
+    if arr.dtype == np.float32:
+        return F32
+    if arr.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits), got {arr.dtype}")
+
+
+def write(k, v, slot_mapping, k_cache, v_cache) -> int:
+    """KV-cache write ("Écriture du KV cache", ch. 6 of the vLLM core book;
+    -1 padding of slot_mapping, ch. 5): copies row t of ``k``/``v`` into cache
+    row ``slot_mapping[t]`` for every slot >= 0, in place.  ``k``/``v`` are
+    [T, Hkv, D], caches [NB, bs, Hkv, D], all float32 or uint16 (bf16 bits).
+    Returns the number of out-of-range slots (skipped)."""
+    lib = _load()
+    k, v = _raw(k), _raw(v)
+    slots = _raw(np.asarray(slot_mapping, dtype=np.int64))
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    nb, bs, hkv, d = k_cache.shape
+    return int(lib.orc_write(_ptr(k), _ptr(v), _ptr(slots), slots.shape[0],
+                             _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d,
+                             k_cache.dtype.itemsize))
+
+
+class Problem:
+    """Keeps the numpy buffers of one attention problem alive for ctypes."""
+
+    def __init__(self, q, k_cache, v_cache, block_tables, context_lens,
+                 query_start_loc, scale):
+        self.q = _raw(q)
+        self.k_cache = _raw(k_cache)
+        self.v_cache = _raw(v_cache)
+        self.block_tables = _raw(np.asarray(block_tables, dtype=np.int32))
+        self.context_lens = _raw(np.asarray(context_lens, dtype=np.int32))
+        self.query_start_loc = _raw(np.asarray(query_start_loc, dtype=np.int32))
+        code = dtype_code(self.q)
+        assert dtype_code(self.k_cache) == code == dtype_code(self.v_cache)
+        nb, bs, hkv, d = self.k_cache.shape
+        self.num_tokens, hq, dq = self.q.shape
+        assert dq == d and hq % hkv == 0
+        s = self.context_lens.shape[0]
+        assert self.query_start_loc.shape[0] == s + 1
+        self.shape = dict(S=s, Hq=hq, Hkv=hkv, D=d, bs=bs, NB=nb)
+        self.c = OrcProblem(
+            _ptr(self.q), _ptr(self.k_cache), _ptr(self.v_cache),
+            _ptr(self.block_tables), _ptr(self.context_lens), _ptr(self.query_start_loc),
+            self.block_tables.shape[1] if self.block_tables.ndim == 2 else 0,
+            s, hq, hkv, d, bs, nb, code, float(scale))
+
+
+def attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+              scale, nthreads: int = 0):
+    """Exact paged attention in fp64 (ch. 6 "Structure des métadonnées",
+    "Flux des paramètres du chemin non-cascadé", "Branche de masque").
+
+    Returns ``(out, seq_status)``: ``out`` is float64 [T, Hq, D]; rows of a
+    sequence with status 1 (metadata error) are zero, status 2 (block id out of
+    range) NaN."""
+    lib = _load()
+    P = Problem(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale)
+    out = np.zeros((P.num_tokens, P.shape["Hq"], P.shape["D"]), dtype=np.float64)
+    status = np.zeros(P.shape["S"], dtype=np.int32)
+    lib.orc_attention(ctypes.byref(P.c), _ptr(out), _ptr(status), int(nthreads))
+    return out, status
+
+
+def row_state(problem: Problem, s: int, hq: int, j: int, p_lo: int = 0,
+              p_hi: int = 2**62):
+    """Unnormalised softmax state (m, l, acc[D]) of one query row over the
+    visible keys in [p_lo, p_hi): the per-split partial of the split buffer
+    (ch. 6 "build() étape par étape", fourth step)."""
+    lib = _load()
+    m = ctypes.c_double()
+    l = ctypes.c_double()
+    acc = np.zeros(problem.shape["D"], dtype=np.float64)
+    st = lib.orc_row_state(ctypes.byref(problem.c), s, hq, j, p_lo, p_hi,
+                           ctypes.byref(m), ctypes.byref(l), _ptr(acc))
+    return st, m.value, l.value, acc
+
+
+def merge(ms, ls, accs):
+    """Merge partial states into one normalised row (merge_attn_states of the
+    ch. 6 sequence diagram)."""
+    lib = _load()
+    m = _raw(np.asarray(ms, dtype=np.float64))
+    l = _raw(np.asarray(ls, dtype=np.float64))
+    a = _raw(np.asarray(accs, dtype=np.float64))
+    n, d = a.shape
+    out = np.zeros(d, dtype=np.float64)
+    lib.orc_merge(n, _ptr(m), _ptr(l), _ptr(a), d, _ptr(out))
+    return out
+
+
+def max_threads() -> int:
+    return int(_load().orc_max_threads())
