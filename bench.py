@@ -1,0 +1,507 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one pass of the whole path over one synthetic decode batch: the KV
+write of this step's new tokens (pkv_write), then paged attention over the
+updated cache (pkv_attention: split-K decode kernel + combine).  The default
+workload is the LLaMA-7B-shaped decode batch (32 q = 32 kv heads, head_size
+128, bf16, 64 sequences, context lengths uniform in [128, 4096]).
+
+Metric: KV bytes moved per second (algorithmic bytes / device time), with the
+fraction of the measured HBM copy bandwidth and decode tokens/s.  Inputs are
+resident in HBM before timing; the KV pool (~2.4 GB) is far larger than L2, so
+no flush is needed between steps.  `--impl reference` times the CPU oracle on
+a bounded sample of the same workload instead.
+
+Launch: `python bench.py [--gpus N --steps K --warmup W]`; for N > 1 under
+torchrun each rank runs its own seeded batch of the same shape (sequences are
+independent: weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged-attn KV GB/s and % of GB300 HBM peak; decode tokens/s at batch"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "paged_kv_cache_43_gb300", "csrc")
+
+
+# ----------------------------------------------------------------- helpers
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("pkv_decode.cu", "pkv_common.cuh", "pkv_internal.h"):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256") != decode_source_hash():
+        return None
+    return rec.get("per_workload", {}).get(workload_name)
+
+
+def algorithmic_bytes(wl):
+    """Bytes the step must move at minimum.
+    attention: each visible K and V row once, q read, out written, the block
+    table entries and per-sequence metadata read;
+    write: new K/V rows read and written, slots read."""
+    e = wl.q.element_size()
+    hkv, d, hq = wl.num_kv_heads, wl.head_size, wl.num_q_heads
+    ctx = wl.ctx_lens.astype(np.int64)
+    kv = int(ctx.sum()) * hkv * d * e * 2
+    qo = 2 * wl.num_tokens * hq * d * e
+    meta = int(np.ceil(ctx / 16).sum()) * 4 + wl.num_seqs * 4 + (wl.num_seqs + 1) * 4
+    attn = kv + qo + meta
+    write = 2 * 2 * wl.num_tokens * hkv * d * e + wl.num_tokens * 8
+    return attn, write, kv
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = str(gpu_index)
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9 or p[0] != self.gpu:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx = max(mx, float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- oracle leg
+
+def oracle_sample(wl_gpu, seqs):
+    """CPU inputs (compact pool) for the sequences `seqs`, including this
+    step's new tokens, for the oracle."""
+    from paged_kv_cache_43_gb300 import workloads as W
+    bt = wl_gpu.block_tables.cpu().numpy()
+    cl = wl_gpu.context_lens.cpu().numpy()
+    qsl = wl_gpu.query_start_loc.cpu().numpy()
+    uniq = sorted({int(b) for s in seqs for b in bt[s, :-(-int(cl[s]) // 16)]})
+    remap = {b: i for i, b in enumerate(uniq)}
+    idx = torch.tensor(uniq, dtype=torch.int64, device=wl_gpu.k_cache.device)
+    kc = W.as_oracle_array(wl_gpu.k_cache.index_select(0, idx)).copy()
+    vc = W.as_oracle_array(wl_gpu.v_cache.index_select(0, idx)).copy()
+    sub_bt = np.full((len(seqs), bt.shape[1]), -1, np.int32)
+    rows, sub_qsl = [], [0]
+    for i, s in enumerate(seqs):
+        nb = -(-int(cl[s]) // 16)
+        sub_bt[i, :nb] = [remap[int(b)] for b in bt[s, :nb]]
+        rows.extend(range(int(qsl[s]), int(qsl[s + 1])))
+        sub_qsl.append(len(rows))
+    rows_t = torch.tensor(rows, dtype=torch.int64, device=wl_gpu.q.device)
+    slots = wl_gpu.slot_mapping.cpu().numpy()[rows]
+    sub_slots = np.array([remap[int(x) // 16] * 16 + int(x) % 16 for x in slots], np.int64)
+    return dict(q=W.as_oracle_array(wl_gpu.q.index_select(0, rows_t)),
+                k_new=W.as_oracle_array(wl_gpu.k_new.index_select(0, rows_t)),
+                v_new=W.as_oracle_array(wl_gpu.v_new.index_select(0, rows_t)),
+                slots=sub_slots, k_cache=kc, v_cache=vc, bt=sub_bt,
+                cl=cl[seqs].astype(np.int32), qsl=np.array(sub_qsl, np.int32),
+                scale=wl_gpu.scale)
+
+
+def oracle_pass(sample):
+    """One oracle step on a sample: its own KV write, then attention."""
+    import oracle
+    kc, vc = sample["k_cache"].copy(), sample["v_cache"].copy()
+    oracle.write(sample["k_new"], sample["v_new"], sample["slots"], kc, vc)
+    out, st = oracle.attention(sample["q"], kc, vc, sample["bt"], sample["cl"], sample["qsl"],
+                               sample["scale"])
+    return out
+
+
+def sample_bytes(wl, sample):
+    e = wl.q.element_size()
+    keys = int(sample["cl"].sum())
+    t = int(sample["qsl"][-1])
+    return (keys * wl.num_kv_heads * wl.head_size * e * 2 + 2 * t * wl.num_q_heads * wl.head_size * e
+            + 4 * t * wl.num_kv_heads * wl.head_size * e)
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """Oracle on a growing sample of the workload's sequences until about
+    budget_s of CPU time has been spent; GB/s over the sample."""
+    import oracle
+    order = list(np.argsort(wl.ctx_lens))
+    pick, spent, total_bytes, n = [], 0.0, 0, 1
+    while spent < budget_s and len(pick) < len(order):
+        new = [int(x) for x in order[len(pick)::max(1, len(order) // 8)][:n]]
+        new = [s for s in new if s not in pick] or [int(order[len(pick)])]
+        smp = oracle_sample(wl, sorted(new))
+        t0 = time.perf_counter()
+        oracle_pass(smp)
+        dt = time.perf_counter() - t0
+        spent += dt
+        total_bytes += sample_bytes(wl, smp)
+        pick.extend(new)
+        n *= 2
+    return {"value": total_bytes / spent / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{len(pick)} of {wl.num_seqs} sequences (all heads) of {wl.name}: "
+                      f"fp64 KV write + attention, {spent:.1f} s of CPU"}
+
+
+# ----------------------------------------------------------------- arms
+
+def run_pkv(args, rank, world, device):
+    from paged_kv_cache_43_gb300 import build, pkv
+    from paged_kv_cache_43_gb300 import workloads as W
+
+    build.build()
+    pkv.load()
+    wl = W.workload(args.workload, device=device, seed=W.SEED_BASE + args.workload + 1000 * rank)
+    attn_b, write_b, kv_b = algorithmic_bytes(wl)
+    step_b = attn_b + write_b
+    out = torch.empty_like(wl.q)
+    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, max_query_len=wl.max_query_len,
+                         max_context_len=wl.max_context_len, num_decode_seqs=wl.num_decode_seqs,
+                         kv_split_tokens=args.kv_split)
+    ws_n = pkv.workspace_size(wl.k_cache, meta)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    max_splits = 0
+    if ws_n:
+        max_splits = 1  # combine launched
+    launches_per_step = 1 + 1 + (1 if ws_n else 0) + (1 if wl.num_decode_seqs < wl.num_seqs else 0)
+
+    def step():
+        pkv.run_step(wl, out, workspace=ws, kv_split_tokens=args.kv_split, stream=stream)
+
+    pkv.get_error(clear=True)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    if pkv.get_error(clear=True):
+        raise RuntimeError("device error word set during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        pkv.write(wl.k_new, wl.v_new, wl.slot_mapping, wl.k_cache, wl.v_cache, stream=stream)
+        e1.record(stream)
+        pkv.attention(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
+                      wl.query_start_loc, wl.scale, max_query_len=wl.max_query_len,
+                      max_context_len=wl.max_context_len, num_decode_seqs=wl.num_decode_seqs,
+                      kv_split_tokens=args.kv_split, workspace=ws, stream=stream)
+        e2.record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    total_ms = start.elapsed_time(end)
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    if pkv.get_error(clear=True):
+        raise RuntimeError("device error word set during the timed region")
+    # parity spot check on the timed output: a few rows against the oracle
+    parity = spot_check(wl, out)
+
+    t = torch.tensor([total_ms], device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # ---- end to end: host buffers in, host result out, same stream
+    e2e = end_to_end(wl, args, stream, device, step_b)
+
+    if rank != 0:
+        return None
+    peak, peak_kind = hbm_peak()
+    value = world * step_b / (ms_per_step * 1e-3) / 1e9
+    achieved = attn_b / (attn_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) q/k/v, random block placement)",
+        "config": {
+            "workload": wl.name,
+            "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_size": wl.head_size, "block_size": 16,
+            "context_lens": f"{int(wl.ctx_lens.min())}..{int(wl.ctx_lens.max())} "
+                            f"(mean {wl.ctx_lens.mean():.0f})",
+            "max_query_len": wl.max_query_len, "num_tokens": wl.num_tokens,
+            "kv_split_tokens": args.kv_split or "auto",
+            "step": "pkv_write of the new tokens + pkv_attention",
+            "l2": f"inputs larger than L2: {kv_b / 1e9:.2f} GB of K/V read per step, no flush",
+            "parallelism": f"replicas x{world} (independent sequence batches)",
+        },
+        "pct_hbm_peak": round(100.0 * value / world / peak, 1),
+        "decode_tokens_per_s": round(world * wl.num_tokens / (ms_per_step * 1e-3), 1),
+        "attention_ms": round(attn_ms, 5),
+        "write_ms": round(write_ms, 5),
+        "roofline": {
+            "kernel": "pkv_attention (split-K decode kernel + combine), CUDA events per call",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": attn_b,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "parity_max_abs_err": parity,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    return line
+
+
+def spot_check(wl, out):
+    """Max |error| of a few timed output rows against the oracle."""
+    import oracle
+    seqs = [int(np.argmin(wl.ctx_lens)), int(np.argmax(wl.ctx_lens))]
+    # the cache already holds this step's tokens; rebuild the sample from the
+    # pre-write view by letting the oracle rewrite the same rows (idempotent)
+    smp = oracle_sample(wl, seqs)
+    exp = oracle_pass(smp)
+    rows = []
+    qsl = wl.query_start_loc.cpu().numpy()
+    for s in seqs:
+        rows.extend(range(int(qsl[s]), int(qsl[s + 1])))
+    got = out[torch.tensor(rows, device=out.device)].float().cpu().numpy().astype(np.float64)
+    err = float(np.abs(got - exp).max())
+    if not (err <= (2e-2 if wl.dtype == torch.bfloat16 else 1e-5)):
+        raise RuntimeError(f"timed output fails parity: max abs err {err}")
+    return err
+
+
+def end_to_end(wl, args, stream, device, step_bytes):
+    """Same metric through the public calls with host-resident step inputs:
+    pinned H2D of q, new K/V, slots and metadata, the step, D2H of out."""
+    from paged_kv_cache_43_gb300 import pkv
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
+             "query_start_loc")
+    host = {n: getattr(wl, n).cpu().pin_memory() for n in names}
+    dev = {n: torch.empty_like(getattr(wl, n)) for n in names}
+    out_h = torch.empty(wl.q.shape, dtype=wl.q.dtype).pin_memory()
+    out_d = torch.empty_like(wl.q)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    meta_kw = dict(max_query_len=wl.max_query_len, max_context_len=wl.max_context_len,
+                   num_decode_seqs=wl.num_decode_seqs, kv_split_tokens=args.kv_split)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for n in names:
+                dev[n].copy_(host[n], non_blocking=True)
+        pkv.write(dev["k_new"], dev["v_new"], dev["slot_mapping"], wl.k_cache, wl.v_cache,
+                  stream=stream)
+        pkv.attention(out_d, dev["q"], wl.k_cache, wl.v_cache, dev["block_tables"],
+                      dev["context_lens"], dev["query_start_loc"], wl.scale, stream=stream,
+                      **meta_kw)
+        with torch.cuda.stream(stream):
+            out_h.copy_(out_d, non_blocking=True)
+
+    n = max(args.steps // 4, 10)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / n
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
+            "steps": n}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is the oracle's KV write +
+    attention on a bounded sample of the same workload (generated on the GPU
+    with the same seed, copied to the host)."""
+    if rank != 0:
+        return None
+    from paged_kv_cache_43_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    wl = W.workload(args.workload, device=device)
+    attn_b, write_b, _ = algorithmic_bytes(wl)
+    # pick the sample so that warmup + steps fit in about budget seconds
+    budget = float(os.environ.get("PKV_REFERENCE_BUDGET_S", "150"))
+    order = [int(x) for x in np.argsort(wl.ctx_lens)]
+    smp = oracle_sample(wl, [order[len(order) // 2]])
+    t0 = time.perf_counter()
+    oracle_pass(smp)
+    one = time.perf_counter() - t0
+    per_step = budget / max(args.steps + args.warmup, 1)
+    if one > per_step:
+        # shrink to a head subset of one sequence
+        frac = max(per_step / one, 1.0 / wl.num_q_heads)
+        smp["q"] = smp["q"][:, : max(1, int(wl.num_q_heads * frac)) // (wl.num_q_heads // wl.num_kv_heads) * (wl.num_q_heads // wl.num_kv_heads) or (wl.num_q_heads // wl.num_kv_heads)]
+    for _ in range(args.warmup):
+        oracle_pass(smp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(smp)
+    dt = time.perf_counter() - t0
+    hq_used = smp["q"].shape[1]
+    e = wl.q.element_size()
+    keys = int(smp["cl"].sum())
+    t = int(smp["qsl"][-1])
+    g = wl.num_q_heads // wl.num_kv_heads
+    hkv_used = max(1, hq_used // g)
+    b = keys * hkv_used * wl.head_size * e * 2 + 2 * t * hq_used * wl.head_size * e
+    value = b * args.steps / dt / 1e9
+    ms = dt / args.steps * 1e3
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded workload, bounded sample)", "impl": "reference",
+        "config": {"workload": wl.name, "sample": f"1 sequence ({keys} keys), {hq_used} of "
+                   f"{wl.num_q_heads} q heads per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": f"1 sequence of {wl.name}, {hq_used} heads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--kv-split", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    try:
+        line = run_pkv(args, rank, world, device)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -90,8 +90,12 @@ typedef struct {
   int32_t num_tokens;         /* T = query_start_loc[S] (rows of q and out)     */
   int32_t num_q_heads;        /* Hq, a multiple of num_kv_heads (GQA)           */
   int32_t block_table_stride; /* int32 entries per block_tables row (>= 1)      */
-  int32_t max_query_len;      /* >= every query length; 1 means pure decode     */
-  int32_t max_context_len;    /* >= every context_lens[s]; sizes split-K        */
+  int32_t max_query_len;      /* >= every query length; 1 means pure decode.    */
+                              /* A longer sequence sets PKV_ERR_QUERY_LEN and   */
+                              /* its rows are unspecified                       */
+  int32_t max_context_len;    /* >= every context_lens[s]; sizes split-K.  A    */
+                              /* decode sequence past it sets                   */
+                              /* PKV_ERR_CONTEXT_LEN (rows zero)                */
   int32_t num_decode_seqs;    /* sequences 0..n-1 have query length 1 (the      */
                               /* decode run of a mixed batch); -1 = unknown     */
   int32_t kv_split_tokens;    /* split-K chunk in keys for decode: 0 = choose   */
@@ -137,7 +141,10 @@ size_t pkv_attention_workspace_size(const pkv_cache_desc *cache,
  *   block_tables      int32 [num_seqs, block_table_stride]; entries past
  *                     ceil(L / block_size) are never read
  *   context_lens      int32 [num_seqs]
- *   query_start_loc   int32 [num_seqs + 1], non-decreasing, [0] = 0
+ *   query_start_loc   int32 [num_seqs + 1], non-decreasing, [0] = 0,
+ *                     [num_seqs] <= num_tokens (a sequence whose rows fall
+ *                     outside [0, num_tokens) sets PKV_ERR_QUERY_LEN and is
+ *                     skipped)
  *   workspace         device scratch of at least
  *                     pkv_attention_workspace_size() bytes (may be NULL when
  *                     that is 0); its contents need no initialisation.

@@ -1,0 +1,323 @@
+// pkv_api.cu -- the C ABI of include/pkv.h: host-side argument checks, the
+// split-K plan, TMA descriptor encoding and kernel dispatch.
+//
+// Nothing here allocates device memory or synchronises, except
+// pkv_get_error(), which is documented as synchronising.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+// Per-device error word (PKV_ERR_* bits), OR-ed by the kernels.
+__device__ int32_t g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int32_t* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Device-side address of the error word and the SM count, once per device.
+int device_state(int32_t** err, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_E_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return PKV_E_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKV_E_CUDA;
+    g_err_ptr[dev] = static_cast<int32_t*>(p);
+    g_num_sms[dev] = sms;
+  }
+  *err = g_err_ptr[dev];
+  *num_sms = g_num_sms[dev];
+  return PKV_OK;
+}
+
+int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || f == nullptr)
+      return PKV_E_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *fn = g_encode;
+  return PKV_OK;
+}
+
+// TMA descriptor of one bf16 cache viewed as a 3-D tensor
+// (head_size, num_kv_heads, num_blocks * 16) with a box of 64 columns x 1 head
+// x 16 rows (one cache block of one head, 128 bytes wide) and the 128-byte
+// swizzle.
+int encode_cache_map(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  if (int st = encode_fn(&fn)) return st;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c.head_size),
+                              static_cast<cuuint64_t>(c.num_kv_heads),
+                              static_cast<cuuint64_t>(c.num_blocks) * c.block_size};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.head_size) * 2,
+                                 static_cast<cuuint64_t>(c.num_kv_heads) * c.head_size * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(c.block_size)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_cache(const pkv_cache_desc* c) {
+  if (c == nullptr) return PKV_E_NULL;
+  if (c->dtype != PKV_F32 && c->dtype != PKV_BF16) return PKV_E_DTYPE;
+  if (c->block_size != kBlock) return PKV_E_SHAPE;
+  if (c->head_size != 64 && c->head_size != 128) return PKV_E_SHAPE;
+  if (c->num_kv_heads < 1 || c->num_blocks < 0) return PKV_E_SHAPE;
+  // TMA coordinates of cache rows are int32.
+  if (static_cast<int64_t>(c->num_blocks) * c->block_size > INT32_MAX) return PKV_E_SHAPE;
+  return PKV_OK;
+}
+
+// How the batch is cut: decode run, prefill rest, split-K chunk.
+struct Plan {
+  int num_decode = 0;     // sequences [0, num_decode) go to the decode kernel
+  int split_blocks = 0;   // cache blocks per decode split
+  int max_splits = 0;
+  size_t ws_o_bytes = 0;  // fp32 partial outputs
+  size_t ws_bytes = 0;    // total workspace
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan* p) {
+  if (int st = check_cache(c)) return st;
+  if (m == nullptr) return PKV_E_NULL;
+  if (m->num_seqs < 0 || m->num_tokens < 0 || m->max_query_len < 0 || m->max_context_len < 0 ||
+      m->block_table_stride < 1)
+    return PKV_E_META;
+  if (m->num_q_heads < 1 || m->num_q_heads % c->num_kv_heads != 0) return PKV_E_GQA;
+  if (m->num_q_heads > 65535) return PKV_E_SHAPE;
+  if (m->num_decode_seqs < -1 || m->num_decode_seqs > m->num_seqs) return PKV_E_META;
+  if (m->kv_split_tokens != 0 &&
+      (m->kv_split_tokens < 64 || m->kv_split_tokens > 2048 || m->kv_split_tokens % 64 != 0))
+    return PKV_E_META;
+  *p = Plan{};
+  if (c->dtype == PKV_F32) return PKV_OK;  // one kernel, no workspace
+  int nd = 0;
+  if (m->max_query_len <= 1) nd = m->num_seqs;
+  else if (m->num_decode_seqs >= 0) nd = m->num_decode_seqs;
+  p->num_decode = nd;
+  if (nd == 0) return PKV_OK;
+  const int max_blocks = (m->max_context_len + kBlock - 1) / kBlock;
+  int split_blocks;
+  if (m->kv_split_tokens > 0) {
+    split_blocks = m->kv_split_tokens / kBlock;
+  } else {
+    // 512-key chunks (256 KB of K+V per head at D=128) balance the uneven
+    // context lengths of a decode batch; shorter chunks only when the batch
+    // has too few (sequence, head) units to fill the GPU twice over.
+    const int g_sub = (m->num_q_heads / c->num_kv_heads + 7) / 8;
+    const int64_t units = static_cast<int64_t>(nd) * c->num_kv_heads * g_sub;
+    const int64_t want = 2LL * num_sms * 2;  // two waves of two CTAs per SM
+    split_blocks = 32;
+    while (split_blocks > 4 &&
+           units * ((max_blocks + split_blocks - 1) / split_blocks) < want)
+      split_blocks /= 2;
+  }
+  p->split_blocks = split_blocks;
+  p->max_splits = max_blocks > 0 ? (max_blocks + split_blocks - 1) / split_blocks : 1;
+  if (p->max_splits > 1) {
+    const size_t rows = static_cast<size_t>(nd) * m->num_q_heads * p->max_splits;
+    p->ws_o_bytes = round_up(rows * c->head_size * sizeof(float), 256);
+    p->ws_bytes = p->ws_o_bytes + round_up(rows * sizeof(float), 256);
+  }
+  return PKV_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int pkv_write(const void* k, const void* v, const int64_t* slot_mapping,
+                         int32_t num_tokens, void* k_cache, void* v_cache,
+                         const pkv_cache_desc* cache, void* stream) {
+  if (int st = check_cache(cache)) return st;
+  if (num_tokens < 0) return PKV_E_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_E_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PKV_E_ALIGN;
+  int32_t* err;
+  int sms;
+  if (int st = device_state(&err, &sms)) return st;
+  const int ebytes = cache->dtype == PKV_BF16 ? 2 : 4;
+  WriteArgs a;
+  a.k = k;
+  a.v = v;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.err = err;
+  a.num_slots = static_cast<int64_t>(cache->num_blocks) * cache->block_size;
+  a.num_tokens = num_tokens;
+  a.row_vecs = cache->num_kv_heads * cache->head_size * ebytes / 16;
+  return launch_write(a, as_stream(stream), sms) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+}
+
+extern "C" size_t pkv_attention_workspace_size(const pkv_cache_desc* cache,
+                                               const pkv_attn_meta* meta) {
+  int32_t* err;
+  int sms;
+  if (device_state(&err, &sms) != PKV_OK) return static_cast<size_t>(-1);
+  Plan p;
+  if (make_plan(cache, meta, sms, &p) != PKV_OK) return static_cast<size_t>(-1);
+  return p.ws_bytes;
+}
+
+extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             const int32_t* query_start_loc, float scale,
+                             const pkv_cache_desc* cache, const pkv_attn_meta* meta,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t* err;
+  int sms;
+  if (int st = device_state(&err, &sms)) return st;
+  Plan p;
+  if (int st = make_plan(cache, meta, sms, &p)) return st;
+  if (meta->num_seqs == 0 || meta->num_tokens == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start_loc)
+    return PKV_E_NULL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u))
+    return PKV_E_ALIGN;
+  if (p.ws_bytes > 0) {
+    if (workspace == nullptr || workspace_bytes < p.ws_bytes) return PKV_E_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_E_ALIGN;
+  }
+  const cudaStream_t st = as_stream(stream);
+  const float LOG2E = 1.4426950408889634f;
+
+  if (cache->dtype == PKV_F32) {
+    F32Args a;
+    a.out = static_cast<float*>(out);
+    a.q = static_cast<const float*>(q);
+    a.k_cache = static_cast<const float*>(k_cache);
+    a.v_cache = static_cast<const float*>(v_cache);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start_loc = query_start_loc;
+    a.err = err;
+    a.bt_stride = meta->block_table_stride;
+    a.num_seqs = meta->num_seqs;
+    a.num_tokens = meta->num_tokens;
+    a.num_q_heads = meta->num_q_heads;
+    a.num_kv_heads = cache->num_kv_heads;
+    a.head_size = cache->head_size;
+    a.num_blocks = cache->num_blocks;
+    a.scale = scale;
+    return launch_attention_f32(a, st) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+  }
+
+  if (cache->num_blocks == 0) return PKV_E_SHAPE;
+  CUtensorMap kmap, vmap;
+  if (int e = encode_cache_map(&kmap, k_cache, *cache)) return e;
+  if (int e = encode_cache_map(&vmap, v_cache, *cache)) return e;
+  const int G = meta->num_q_heads / cache->num_kv_heads;
+
+  if (p.num_decode > 0) {
+    DecodeArgs d;
+    d.out = out;
+    d.q = q;
+    d.block_tables = block_tables;
+    d.context_lens = context_lens;
+    d.query_start_loc = query_start_loc;
+    d.ws_o = p.ws_bytes ? static_cast<float*>(workspace) : nullptr;
+    d.ws_lse = p.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ws_o_bytes)
+                          : nullptr;
+    d.err = err;
+    d.bt_stride = meta->block_table_stride;
+    d.num_seqs = p.num_decode;
+    d.num_q_heads = meta->num_q_heads;
+    d.num_kv_heads = cache->num_kv_heads;
+    d.group = G;
+    d.num_blocks = cache->num_blocks;
+    d.split_blocks = p.split_blocks;
+    d.max_splits = p.max_splits;
+    d.num_tokens = meta->num_tokens;
+    d.max_context_len = meta->max_context_len;
+    d.scale_log2 = scale * LOG2E;
+    if (launch_decode_bf16(kmap, vmap, d, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
+    if (launch_combine_bf16(d, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
+  }
+  const int npf = meta->num_seqs - p.num_decode;
+  if (npf > 0) {
+    PrefillArgs f;
+    f.out = out;
+    f.q = q;
+    f.block_tables = block_tables;
+    f.context_lens = context_lens;
+    f.query_start_loc = query_start_loc;
+    f.err = err;
+    f.bt_stride = meta->block_table_stride;
+    f.seq_begin = p.num_decode;
+    f.num_seqs = npf;
+    f.num_q_heads = meta->num_q_heads;
+    f.num_kv_heads = cache->num_kv_heads;
+    f.group = G;
+    f.num_blocks = cache->num_blocks;
+    const int64_t rows = static_cast<int64_t>(meta->max_query_len) * G;
+    f.num_mtiles = static_cast<int32_t>((rows + kPrefillRows - 1) / kPrefillRows);
+    f.num_tokens = meta->num_tokens;
+    f.max_query_len = meta->max_query_len;
+    f.scale_log2 = scale * LOG2E;
+    if (launch_prefill_bf16(kmap, vmap, f, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
+  }
+  return PKV_OK;
+}
+
+extern "C" int pkv_get_error(int32_t* error_bits, int clear) {
+  if (error_bits == nullptr) return PKV_E_NULL;
+  int32_t* err;
+  int sms;
+  if (int st = device_state(&err, &sms)) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_E_CUDA;
+  if (cudaMemcpy(error_bits, err, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PKV_E_CUDA;
+  if (clear && cudaMemset(err, 0, sizeof(int32_t)) != cudaSuccess) return PKV_E_CUDA;
+  if (clear && cudaDeviceSynchronize() != cudaSuccess) return PKV_E_CUDA;
+  return PKV_OK;
+}
+
+extern "C" const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_E_NULL: return "a required pointer is NULL";
+    case PKV_E_DTYPE: return "unsupported dtype (PKV_F32 or PKV_BF16)";
+    case PKV_E_SHAPE: return "unsupported or out-of-range shape (block_size 16, head_size 64/128)";
+    case PKV_E_GQA: return "num_q_heads is not a multiple of num_kv_heads";
+    case PKV_E_WORKSPACE: return "workspace missing or smaller than pkv_attention_workspace_size";
+    case PKV_E_ALIGN: return "pointer not aligned (16 B tensors, 4 B int32 metadata, 256 B workspace)";
+    case PKV_E_CUDA: return "CUDA launch or driver call failed";
+    case PKV_E_META: return "inconsistent pkv_attn_meta";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,432 @@
+// pkv_decode.cu -- paged decode attention (one query row per sequence), bf16,
+// with split-K over the context and the log-sum-exp combine.
+//
+// What it computes: for each decode sequence s (context length L), kv head h
+// and the G query heads of h (GQA, contiguous groups), the exact softmax
+// attention of the query over keys 0..L-1, each fetched from block
+// block_tables[s][p / 16] at offset p % 16 -- "Implémentation du cœur du
+// moteur d'inférence haute performance vLLM", ch. 6 "Flux des paramètres du
+// chemin non-cascadé" (seqused_k = seq_lens, block_table) and "Transformation
+// de la disposition mémoire du KV cache" ([num_blocks, 16, Hkv, D] layout).
+// Long contexts are split into chunks whose fp32 partial outputs and
+// log-sum-exps go to a caller-provided buffer (ch. 6 "build() étape par
+// étape", fourth step) and are merged by a second kernel (merge_attn_states in
+// the ch. 6 sequence diagram).
+//
+// GB300 design (HBM-bound: every K/V byte is read once):
+//  * grid = (split, kv head x 8-head group, sequence); 4 warps per CTA, each
+//    warp owns every 4th cache block of the split and runs its own NS-deep
+//    TMA ring: one 16-key block of K and of V (2 x 16 x D bf16) per stage,
+//    loaded as 64-column boxes with the 128-byte swizzle (conflict-free
+//    ldmatrix), completion on a per-stage mbarrier, evict-first L2 policy.
+//  * keys sit on the MMA's M dimension and the query heads of the group on N:
+//    S^T[16 keys x 8 heads] = K_blk . Q^T (m16n8k16, Q^T held in registers),
+//    so one tile serves all G <= 8 heads and no head padding to 16 is needed.
+//    The probabilities are rounded to bf16, transposed in registers
+//    (movmatrix) into the B operand of O^T[D x 8] += V_blk^T . P^T
+//    (ldmatrix.trans of the same swizzled V tile).  Online softmax in the
+//    log2 domain; the denominator sums the same rounded weights the MMA uses.
+//  * warps merge through shared memory; a CTA whose sequence needs one split
+//    writes bf16 output, otherwise an fp32 partial + log-sum-exp.
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kDecodeWarps = 4;
+
+template <int D>
+struct DecodeTile {
+  static constexpr int kHalves = D / 64;           // 64-column TMA boxes per row
+  static constexpr int kTileBytes = D * 2 * kBlock;  // one 16-key block of K (or V)
+  static constexpr int kStageBytes = 2 * kTileBytes;
+};
+
+template <int D, int NS>
+constexpr int decode_smem_bytes() {
+  return 1024 /* alignment slack */ + kDecodeWarps * NS * DecodeTile<D>::kStageBytes +
+         kDecodeWarps * NS * 8 /* mbarriers */ + 2 * kDecodeWarps * 8 * 4 /* merge factors */;
+}
+
+template <int D, int NS>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    pkv_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
+                           const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+  using T = DecodeTile<D>;
+  constexpr int NW = kDecodeWarps;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NS * T::kStageBytes);
+  float* merge_f = reinterpret_cast<float*>(bars + NW * NS);  // [NW][8] factors, [8] lse
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int s = blockIdx.z;
+  const int ngsub = (a.group + 7) >> 3;
+  const int kvh = blockIdx.y / ngsub;
+  const int gsub = blockIdx.y - kvh * ngsub;
+  const int G = a.group;
+  const int Hq = a.num_q_heads;
+  const bool reporter = (split == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+
+  const int L = __ldg(a.context_lens + s);
+  const int q0 = __ldg(a.query_start_loc + s);
+  const int qn = __ldg(a.query_start_loc + s + 1) - q0;
+  if (qn != 1 || q0 < 0 || q0 >= a.num_tokens) {
+    if (qn != 0 && reporter) raise_error(a.err, qn == 1 ? PKV_ERR_QUERY_LEN : PKV_ERR_DECODE_QLEN);
+    return;
+  }
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  if (L < 1 || static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len) {
+    if (reporter) raise_error(a.err, PKV_ERR_CONTEXT_LEN);
+    if (split == 0) {  // zero rows for a sequence with bad metadata
+      for (int i = threadIdx.x; i < 8 * D; i += NW * 32) {
+        const int g = gsub * 8 + i / D;
+        if (g < G) out[(static_cast<int64_t>(q0) * Hq + kvh * G + g) * D + (i % D)] =
+            __float2bfloat16(0.f);
+      }
+    }
+    return;
+  }
+  const int nblk_seq = (L + kBlock - 1) / kBlock;
+  const int nsplit = (nblk_seq + a.split_blocks - 1) / a.split_blocks;
+  if (split >= nsplit) return;
+  const int b_begin = split * a.split_blocks;
+  const int b_end = min(b_begin + a.split_blocks, nblk_seq);
+  const int nblk = b_end - b_begin;
+  const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;  // <= 32 by construction
+
+  if (threadIdx.x == 0) {
+    prefetch_tensor_map(&kmap);
+    prefetch_tensor_map(&vmap);
+  }
+
+  // Block ids of this warp's blocks: lane i holds its i-th block.
+  int my_bid = -1;
+  if (lane < nb_w)
+    my_bid = __ldg(a.block_tables + static_cast<int64_t>(s) * a.bt_stride + b_begin + warp +
+                   NW * lane);
+  const bool my_ok = (my_bid >= 0 && my_bid < a.num_blocks);
+  if (lane < nb_w && !my_ok) raise_error(a.err, PKV_ERR_BLOCK_ID);
+
+  uint8_t* wbase = smem + warp * NS * T::kStageBytes;
+  const uint32_t wbase_u = smem_u32(wbase);
+  const uint32_t bar0 = smem_u32(bars + warp * NS);
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < NS; ++st) mbar_init(bar0 + 8 * st, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  const uint64_t policy = policy_evict_first();
+  // Issues this warp's block i into stage i % NS (all lanes call; lane 0 acts).
+  auto issue = [&](int i) {
+    const int bid = __shfl_sync(0xffffffffu, my_bid, i);
+    const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
+    if (lane == 0) {
+      const int st = i % NS;
+      const uint32_t dst = wbase_u + st * T::kStageBytes;
+      const uint32_t bar = bar0 + 8 * st;
+      if (ok) {
+        mbar_arrive_expect_tx(bar, T::kStageBytes);
+#pragma unroll
+        for (int h = 0; h < T::kHalves; ++h) {
+          tma_load_3d(dst + h * 2048, &kmap, bar, h * 64, kvh, bid * kBlock, policy);
+          tma_load_3d(dst + T::kTileBytes + h * 2048, &vmap, bar, h * 64, kvh, bid * kBlock,
+                      policy);
+        }
+      } else {
+        mbar_arrive(bar);  // nothing to load: complete the phase empty
+      }
+    }
+  };
+
+  const int n_pro = nb_w < NS ? nb_w : NS;
+  for (int i = 0; i < n_pro; ++i) issue(i);
+  int issued = n_pro;  // blocks whose copies have been started
+
+  // Q^T as the B operand: lane holds Q[g = lane/4][kk*16 + 2*(lane%4) + {0,1}]
+  // (qb[kk][0]) and the same +8 (qb[kk][1]); heads past the group are zero.
+  uint32_t qb[D / 16][2];
+  {
+    const int g = gsub * 8 + (lane >> 2);
+    const bool gv = g < G;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        static_cast<const __nv_bfloat16*>(a.q) +
+        (static_cast<int64_t>(q0) * Hq + kvh * G + (gv ? g : 0)) * D);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qb[kk][0] = gv ? __ldg(qrow + kk * 8 + (lane & 3)) : 0u;
+      qb[kk][1] = gv ? __ldg(qrow + kk * 8 + 4 + (lane & 3)) : 0u;
+    }
+  }
+
+  float o[D / 16][4];
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY};
+  float l[2] = {0.f, 0.f};
+
+  // Per-lane ldmatrix row/column pieces.
+  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8;   // QK: A = K (keys x d)
+  const int k_dsub = (lane >> 4) * 8;
+  const int v_row = (lane & 7) + ((lane >> 4) & 1) * 8;   // PV: A = V^T via .trans
+  const int v_dsub = ((lane >> 3) & 1) * 8;
+  const int r0 = lane >> 2;                                // score rows (keys) r0, r0 + 8
+  bool timed_out = false;
+
+  for (int i = 0; i < nb_w; ++i) {
+    const int st = i % NS;
+    const uint32_t kbuf = wbase_u + st * T::kStageBytes;
+    const uint32_t vbuf = kbuf + T::kTileBytes;
+    const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
+    if (!mbar_wait(bar0 + 8 * st, (i / NS) & 1)) {
+      timed_out = true;
+      break;
+    }
+    if (ok) {
+      const int p0 = (b_begin + warp + NW * i) * kBlock;  // first key of the block
+      // ---- S^T = K . Q^T  (16 keys x 8 heads)
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kbuf + swz_offset(k_row, kk * 16 + k_dsub), a0, a1, a2, a3);
+        mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      }
+      // ---- mask keys past the context (they may hold stale NaN)
+      const bool v0 = p0 + r0 < L, v1 = p0 + r0 + 8 < L;
+      float x[4];
+      x[0] = v0 ? sc[0] * a.scale_log2 : -INFINITY;
+      x[1] = v0 ? sc[1] * a.scale_log2 : -INFINITY;
+      x[2] = v1 ? sc[2] * a.scale_log2 : -INFINITY;
+      x[3] = v1 ? sc[3] * a.scale_log2 : -INFINITY;
+      // ---- online softmax per head column c (keys spread over lane/4)
+      float alpha[2];
+      uint32_t pk0, pk1;
+      {
+        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        alpha[0] = exp2f(m[0] - mu0);
+        alpha[1] = exp2f(m[1] - mu1);
+        m[0] = mn0;
+        m[1] = mn1;
+        pk0 = pack_bf16(exp2f(x[0] - mu0), exp2f(x[1] - mu1));  // key r0, heads c0,c1
+        pk1 = pack_bf16(exp2f(x[2] - mu0), exp2f(x[3] - mu1));  // key r0+8
+        l[0] = l[0] * alpha[0] + bf16_lo(pk0) + bf16_lo(pk1);
+        l[1] = l[1] * alpha[1] + bf16_hi(pk0) + bf16_hi(pk1);
+      }
+#pragma unroll
+      for (int dt = 0; dt < D / 16; ++dt) {
+        o[dt][0] *= alpha[0];
+        o[dt][1] *= alpha[1];
+        o[dt][2] *= alpha[0];
+        o[dt][3] *= alpha[1];
+      }
+      const uint32_t pb0 = movmatrix_trans(pk0);  // P^T rows = heads, keys 0..7
+      const uint32_t pb1 = movmatrix_trans(pk1);  // keys 8..15
+      // ---- the sequence's last, partial block: zero V rows past the context
+      if (p0 + kBlock > L) {
+        const int nvalid = L - p0;
+        uint8_t* vrow = wbase + st * T::kStageBytes + T::kTileBytes;
+        for (int e = lane; e < (kBlock - nvalid) * T::kHalves * 8; e += 32) {
+          const int r = nvalid + e / (T::kHalves * 8);
+          const int rem = e % (T::kHalves * 8);
+          *reinterpret_cast<uint4*>(vrow + (rem >> 3) * 2048 + r * 128 + (rem & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async();  // before any later TMA write to this stage
+        __syncwarp();
+      }
+      // ---- O^T += V^T . P^T
+#pragma unroll
+      for (int dt = 0; dt < D / 16; ++dt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(vbuf + swz_offset(v_row, dt * 16 + v_dsub), a0, a1, a2, a3);
+        mma_bf16_16816(o[dt], a0, a1, a2, a3, pb0, pb1);
+      }
+    }
+    __syncwarp();
+    if (i + NS < nb_w) {
+      if (lane == 0) fence_proxy_async();
+      issue(i + NS);
+      ++issued;
+    }
+  }
+
+  if (timed_out) {
+    if (lane == 0) raise_error(a.err, PKV_ERR_TIMEOUT);
+    // Let every copy this warp issued land before the CTA's memory is released.
+    for (int st = 0; st < NS && st < issued; ++st) {
+      const int last = ((issued - 1 - st) / NS) * NS + st;  // last block issued into stage st
+      (void)mbar_wait(bar0 + 8 * st, (last / NS) & 1);
+    }
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  // Denominators: sum the per-lane parts over the 8 lanes sharing a column.
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+  }
+
+  // ---- merge the warps through shared memory (each warp reuses its stage 0)
+  float* wo = reinterpret_cast<float*>(wbase);  // [8 heads][D] then m[8], l[8]
+#pragma unroll
+  for (int dt = 0; dt < D / 16; ++dt) {
+    const int d = dt * 16 + r0;
+    const int c = 2 * (lane & 3);
+    wo[c * D + d] = o[dt][0];
+    wo[(c + 1) * D + d] = o[dt][1];
+    wo[c * D + d + 8] = o[dt][2];
+    wo[(c + 1) * D + d + 8] = o[dt][3];
+  }
+  if (lane < 4) {
+    wo[8 * D + 2 * lane] = m[0];
+    wo[8 * D + 2 * lane + 1] = m[1];
+    wo[8 * D + 8 + 2 * lane] = l[0];
+    wo[8 * D + 8 + 2 * lane + 1] = l[1];
+  }
+  __syncthreads();
+  if (threadIdx.x < 8) {
+    const int c = threadIdx.x;
+    float M = -INFINITY;
+    for (int w = 0; w < NW; ++w)
+      M = fmaxf(M, reinterpret_cast<float*>(smem + w * NS * T::kStageBytes)[8 * D + c]);
+    float den = 0.f;
+    float f[NW];
+    for (int w = 0; w < NW; ++w) {
+      const float* ww = reinterpret_cast<float*>(smem + w * NS * T::kStageBytes);
+      f[w] = (M == -INFINITY) ? 0.f : exp2f(ww[8 * D + c] - M);
+      den += f[w] * ww[8 * D + 8 + c];
+    }
+    for (int w = 0; w < NW; ++w) merge_f[w * 8 + c] = den > 0.f ? f[w] / den : 0.f;
+    merge_f[NW * 8 + c] = den > 0.f ? M + log2f(den) : -INFINITY;
+  }
+  __syncthreads();
+
+  const bool direct = (nsplit == 1);
+  for (int idx = threadIdx.x; idx < 8 * D; idx += NW * 32) {
+    const int c = idx / D;
+    const int d = idx - c * D;
+    const int g = gsub * 8 + c;
+    if (g >= G) continue;
+    float r = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      r += merge_f[w * 8 + c] * reinterpret_cast<float*>(smem + w * NS * T::kStageBytes)[c * D + d];
+    const int hq = kvh * G + g;
+    if (direct) {
+      out[(static_cast<int64_t>(q0) * Hq + hq) * D + d] = __float2bfloat16(r);
+    } else {
+      const int64_t row = (static_cast<int64_t>(s) * Hq + hq) * a.max_splits + split;
+      a.ws_o[row * D + d] = r;
+      if (d == 0) a.ws_lse[row] = merge_f[NW * 8 + c];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- combine
+// One warp per (sequence, q head): out = sum_i 2^(lse_i - M) O_i / sum_i 2^(lse_i - M).
+template <int D>
+__global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs a) {
+  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= a.num_seqs * a.num_q_heads) return;
+  const int s = gw / a.num_q_heads;
+  const int hq = gw - s * a.num_q_heads;
+  const int L = __ldg(a.context_lens + s);
+  const int q0 = __ldg(a.query_start_loc + s);
+  const int qn = __ldg(a.query_start_loc + s + 1) - q0;
+  if (qn != 1 || q0 < 0 || q0 >= a.num_tokens || L < 1 ||
+      static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len)
+    return;
+  const int nsplit = ((L + kBlock - 1) / kBlock + a.split_blocks - 1) / a.split_blocks;
+  if (nsplit <= 1) return;  // the decode kernel wrote this row directly
+  const int64_t row = (static_cast<int64_t>(s) * a.num_q_heads + hq) * a.max_splits;
+  float M = -INFINITY;
+  for (int i = lane; i < nsplit; i += 32) M = fmaxf(M, a.ws_lse[row + i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  constexpr int PER = D / 32;  // elements per lane
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float den = 0.f;
+  if (M != -INFINITY) {
+    for (int i = 0; i < nsplit; ++i) {
+      const float lse = a.ws_lse[row + i];
+      const float w = (lse == -INFINITY) ? 0.f : exp2f(lse - M);
+      den += w;
+      const float* oi = a.ws_o + (row + i) * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(oi);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] += w * oi[e];
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) +
+                       (static_cast<int64_t>(q0) * a.num_q_heads + hq) * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(out + e) =
+        __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+}
+
+template <int D, int NS>
+cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int smem = decode_smem_bytes<D, NS>();
+  auto kfn = pkv_decode_bf16_kernel<D, NS>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int ngsub = (a.group + 7) / 8;
+  dim3 grid(a.max_splits, a.num_kv_heads * ngsub, a.num_seqs);
+  kfn<<<grid, kDecodeWarps * 32, smem, stream>>>(kmap, vmap, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Stages per warp: 3 x 8 KB (head_size 128) keeps 2 CTAs (8 warps, up to 16
+// blocks = 128 KB of K/V) in flight per SM.
+cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               const DecodeArgs& a, int head_size, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  if (head_size == 128) return launch_decode_t<128, 3>(kmap, vmap, a, stream);
+  return launch_decode_t<64, 4>(kmap, vmap, a, stream);
+}
+
+cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.max_splits <= 1) return cudaSuccess;
+  const int warps = a.num_seqs * a.num_q_heads;
+  const int blocks = (warps + 3) / 4;
+  if (head_size == 128)
+    pkv_combine_bf16_kernel<128><<<blocks, 128, 0, stream>>>(a);
+  else
+    pkv_combine_bf16_kernel<64><<<blocks, 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,103 @@
+// pkv_internal.h -- argument blocks and launchers shared between the C-ABI
+// front end (pkv_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Keys per cache block; the only block size the kernels take.
+constexpr int kBlock = 16;
+
+struct WriteArgs {
+  const void* k;
+  const void* v;
+  const int64_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
+  int32_t* err;
+  int64_t num_slots;    // num_blocks * block_size
+  int32_t num_tokens;
+  int32_t row_vecs;     // 16-byte vectors per token row (num_kv_heads*head_size*bytes/16)
+};
+
+// Split-K decode over sequences [0, num_seqs) (each with one query row).
+struct DecodeArgs {
+  void* out;                     // bf16 [T, Hq, D]
+  const void* q;                 // bf16 [T, Hq, D]
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  float* ws_o;                   // [num_seqs, Hq, max_splits, D] fp32 (split > 1 only)
+  float* ws_lse;                 // [num_seqs, Hq, max_splits]   log2-domain
+  int32_t* err;
+  int64_t bt_stride;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;                 // num_q_heads / num_kv_heads
+  int32_t num_blocks;
+  int32_t split_blocks;          // cache blocks per split
+  int32_t max_splits;
+  int32_t num_tokens;            // rows of q/out: query_start_loc must stay inside
+  int32_t max_context_len;       // bound the split buffer was sized for
+  float scale_log2;              // scale * log2(e)
+};
+
+// Varlen causal attention over sequences [seq_begin, seq_begin + num_seqs).
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  int32_t* err;
+  int64_t bt_stride;
+  int32_t seq_begin;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t num_blocks;
+  int32_t num_mtiles;            // grid.x: row tiles of the longest sequence
+  int32_t num_tokens;
+  int32_t max_query_len;
+  float scale_log2;
+};
+
+// fp32 I/O: one CTA per (query row, q head), every sequence.
+struct F32Args {
+  float* out;
+  const float* q;
+  const float* k_cache;
+  const float* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  int32_t* err;
+  int64_t bt_stride;
+  int32_t num_seqs;
+  int32_t num_tokens;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_size;
+  int32_t num_blocks;
+  float scale;
+};
+
+cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream, int num_sms);
+cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               const DecodeArgs& a, int head_size, cudaStream_t stream);
+cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream);
+cudaError_t launch_prefill_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                const PrefillArgs& a, int head_size, cudaStream_t stream);
+cudaError_t launch_attention_f32(const F32Args& a, cudaStream_t stream);
+
+// Rows of the prefill kernel's query tile (grid.x covers ceil(q_len*G / this)).
+constexpr int kPrefillRows = 64;
+
+}  // namespace pkv

@@ -1,0 +1,191 @@
+"""Thin ctypes binding of libpkv (include/pkv.h): argument marshalling only.
+
+Every step of the path runs in the CUDA kernels behind the C ABI; this module
+only checks tensor shapes/dtypes, fills the descriptor structs and passes data
+pointers and the current CUDA stream.  If the library cannot be loaded the
+calls raise: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_lock = threading.Lock()
+_lib = None
+
+PKV_F32, PKV_BF16 = 0, 1
+ERR_SLOT = 1 << 0
+ERR_BLOCK_ID = 1 << 1
+ERR_CONTEXT_LEN = 1 << 2
+ERR_QUERY_LEN = 1 << 3
+ERR_DECODE_QLEN = 1 << 4
+ERR_TIMEOUT = 1 << 5
+EXPORTED = ("pkv_write", "pkv_attention_workspace_size", "pkv_attention",
+            "pkv_get_error", "pkv_status_string")
+
+
+class PkvError(RuntimeError):
+    pass
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_size", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+class AttnMeta(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("block_table_stride", ctypes.c_int32),
+                ("max_query_len", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
+                ("num_decode_seqs", ctypes.c_int32), ("kv_split_tokens", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    from . import build as _b
+    return _b.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libpkv.so (built by ``paged_kv_cache_43_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or library_path()
+        if not os.path.exists(path):
+            raise PkvError(f"libpkv.so not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p
+        lib.pkv_write.restype = ctypes.c_int
+        lib.pkv_write.argtypes = [vp, vp, i64p, i32, vp, vp, ctypes.POINTER(CacheDesc), vp]
+        lib.pkv_attention_workspace_size.restype = ctypes.c_size_t
+        lib.pkv_attention_workspace_size.argtypes = [ctypes.POINTER(CacheDesc),
+                                                     ctypes.POINTER(AttnMeta)]
+        lib.pkv_attention.restype = ctypes.c_int
+        lib.pkv_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                      ctypes.POINTER(CacheDesc), ctypes.POINTER(AttnMeta),
+                                      vp, ctypes.c_size_t, vp]
+        lib.pkv_get_error.restype = ctypes.c_int
+        lib.pkv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_status_string.argtypes = [ctypes.c_int]
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise PkvError(f"pkv status {status}: {load().pkv_status_string(status).decode()}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    if t.dtype == torch.float32:
+        return PKV_F32
+    raise PkvError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    nb, bs, hkv, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d, _dtype_code(k_cache))
+
+
+def _require(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not t.is_cuda:
+        raise PkvError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise PkvError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise PkvError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise PkvError(f"{name} must have {ndim} dims")
+
+
+def write(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """pkv_write: scatter k/v [T, Hkv, D] into the caches at slot_mapping[T]."""
+    lib = load()
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n, dtype=k_cache.dtype)
+    _require(slot_mapping, "slot_mapping", dtype=torch.int64, ndim=1)
+    T = slot_mapping.shape[0]
+    if k.shape[0] < T or v.shape[0] < T:
+        raise PkvError("k/v have fewer rows than slot_mapping")
+    desc = cache_desc(k_cache)
+    _check(lib.pkv_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                         k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+                         _stream(stream)))
+
+
+def attn_meta(q, block_tables, context_lens, *, max_query_len, max_context_len,
+              num_decode_seqs=-1, kv_split_tokens=0) -> AttnMeta:
+    return AttnMeta(int(context_lens.shape[0]), int(q.shape[0]), int(q.shape[1]),
+                    int(block_tables.shape[1]), int(max_query_len), int(max_context_len),
+                    int(num_decode_seqs), int(kv_split_tokens))
+
+
+def workspace_size(k_cache, meta: AttnMeta) -> int:
+    desc = cache_desc(k_cache)
+    n = load().pkv_attention_workspace_size(ctypes.byref(desc), ctypes.byref(meta))
+    if n == ctypes.c_size_t(-1).value:
+        raise PkvError("invalid attention description")
+    return int(n)
+
+
+def attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
+              *, max_query_len, max_context_len, num_decode_seqs=-1, kv_split_tokens=0,
+              workspace=None, stream=None) -> None:
+    """pkv_attention into ``out`` [T, Hq, D].  ``workspace`` (uint8 CUDA tensor)
+    is allocated here when not given and the batch needs split-K scratch."""
+    lib = load()
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n, dtype=k_cache.dtype)
+    _require(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _require(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    _require(query_start_loc, "query_start_loc", dtype=torch.int32, ndim=1)
+    if out.shape != q.shape:
+        raise PkvError("out and q must have the same shape")
+    meta = attn_meta(q, block_tables, context_lens, max_query_len=max_query_len,
+                     max_context_len=max_context_len, num_decode_seqs=num_decode_seqs,
+                     kv_split_tokens=kv_split_tokens)
+    desc = cache_desc(k_cache)
+    need = workspace_size(k_cache, meta)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.pkv_attention(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(),
+                             v_cache.data_ptr(), block_tables.data_ptr(),
+                             context_lens.data_ptr(), query_start_loc.data_ptr(),
+                             float(scale), ctypes.byref(desc), ctypes.byref(meta),
+                             ws_ptr, ws_bytes, _stream(stream)))
+
+
+def get_error(clear: bool = True) -> int:
+    """Device error word (PKV_ERR_* bits); synchronises the device."""
+    bits = ctypes.c_int32(0)
+    _check(load().pkv_get_error(ctypes.byref(bits), int(clear)))
+    return int(bits.value)
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(status).decode()
+
+
+def run_step(wl, out, workspace=None, kv_split_tokens=0, stream=None) -> None:
+    """One pass of the hot path over a workload: the KV write of this step's
+    tokens, then attention over the updated cache."""
+    write(wl.k_new, wl.v_new, wl.slot_mapping, wl.k_cache, wl.v_cache, stream=stream)
+    attention(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
+              wl.query_start_loc, wl.scale, max_query_len=wl.max_query_len,
+              max_context_len=wl.max_context_len, num_decode_seqs=wl.num_decode_seqs,
+              kv_split_tokens=kv_split_tokens, workspace=workspace, stream=stream)
