@@ -21,7 +21,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -151,18 +150,22 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- oracle leg
 
-def oracle_sample(wl_gpu, seqs):
-    """CPU inputs (compact pool) for the sequences `seqs`, including this
-    step's new tokens, for the oracle."""
+def oracle_sample(wl_gpu, seqs, kv_heads=None):
+    """CPU inputs (compact pool) for the sequences `seqs`, with this step's new
+    tokens, for the oracle.  Must be taken before any step has run, so that
+    no oracle input passes through the CUDA path.  `kv_heads` keeps only the
+    first kv heads (and their query-head groups)."""
     from paged_kv_cache_43_gb300 import workloads as W
     bt = wl_gpu.block_tables.cpu().numpy()
     cl = wl_gpu.context_lens.cpu().numpy()
     qsl = wl_gpu.query_start_loc.cpu().numpy()
+    g = wl_gpu.num_q_heads // wl_gpu.num_kv_heads
+    hkv = wl_gpu.num_kv_heads if kv_heads is None else kv_heads
     uniq = sorted({int(b) for s in seqs for b in bt[s, :-(-int(cl[s]) // 16)]})
     remap = {b: i for i, b in enumerate(uniq)}
     idx = torch.tensor(uniq, dtype=torch.int64, device=wl_gpu.k_cache.device)
-    kc = W.as_oracle_array(wl_gpu.k_cache.index_select(0, idx)).copy()
-    vc = W.as_oracle_array(wl_gpu.v_cache.index_select(0, idx)).copy()
+    kc = W.as_oracle_array(wl_gpu.k_cache.index_select(0, idx)[:, :, :hkv]).copy()
+    vc = W.as_oracle_array(wl_gpu.v_cache.index_select(0, idx)[:, :, :hkv]).copy()
     sub_bt = np.full((len(seqs), bt.shape[1]), -1, np.int32)
     rows, sub_qsl = [], [0]
     for i, s in enumerate(seqs):
@@ -173,12 +176,13 @@ def oracle_sample(wl_gpu, seqs):
     rows_t = torch.tensor(rows, dtype=torch.int64, device=wl_gpu.q.device)
     slots = wl_gpu.slot_mapping.cpu().numpy()[rows]
     sub_slots = np.array([remap[int(x) // 16] * 16 + int(x) % 16 for x in slots], np.int64)
-    return dict(q=W.as_oracle_array(wl_gpu.q.index_select(0, rows_t)),
-                k_new=W.as_oracle_array(wl_gpu.k_new.index_select(0, rows_t)),
-                v_new=W.as_oracle_array(wl_gpu.v_new.index_select(0, rows_t)),
+    A = W.as_oracle_array
+    return dict(q=A(wl_gpu.q.index_select(0, rows_t)[:, : hkv * g]),
+                k_new=A(wl_gpu.k_new.index_select(0, rows_t)[:, :hkv]),
+                v_new=A(wl_gpu.v_new.index_select(0, rows_t)[:, :hkv]),
                 slots=sub_slots, k_cache=kc, v_cache=vc, bt=sub_bt,
                 cl=cl[seqs].astype(np.int32), qsl=np.array(sub_qsl, np.int32),
-                scale=wl_gpu.scale)
+                scale=wl_gpu.scale, rows=rows)
 
 
 def oracle_pass(sample):
@@ -186,40 +190,39 @@ def oracle_pass(sample):
     import oracle
     kc, vc = sample["k_cache"].copy(), sample["v_cache"].copy()
     oracle.write(sample["k_new"], sample["v_new"], sample["slots"], kc, vc)
-    out, st = oracle.attention(sample["q"], kc, vc, sample["bt"], sample["cl"], sample["qsl"],
-                               sample["scale"])
+    out, _ = oracle.attention(sample["q"], kc, vc, sample["bt"], sample["cl"], sample["qsl"],
+                              sample["scale"])
     return out
 
 
-def sample_bytes(wl, sample):
-    e = wl.q.element_size()
+def sample_bytes(sample):
+    """Algorithmic bytes of one oracle pass over a sample (same accounting as
+    algorithmic_bytes)."""
+    e = sample["k_cache"].dtype.itemsize
+    hkv, d = sample["k_cache"].shape[2], sample["k_cache"].shape[3]
+    hq = sample["q"].shape[1]
     keys = int(sample["cl"].sum())
     t = int(sample["qsl"][-1])
-    return (keys * wl.num_kv_heads * wl.head_size * e * 2 + 2 * t * wl.num_q_heads * wl.head_size * e
-            + 4 * t * wl.num_kv_heads * wl.head_size * e)
+    return keys * hkv * d * e * 2 + 2 * t * hq * d * e + 4 * t * hkv * d * e
 
 
-def cpu_baseline(wl, budget_s=12.0):
-    """Oracle on a growing sample of the workload's sequences until about
-    budget_s of CPU time has been spent; GB/s over the sample."""
+def cpu_baseline(samples, name, num_seqs, budget_s=12.0):
+    """The oracle, as it stands, over pre-step samples of the workload (one
+    sequence each, all heads) until about budget_s of CPU time is spent."""
     import oracle
-    order = list(np.argsort(wl.ctx_lens))
-    pick, spent, total_bytes, n = [], 0.0, 0, 1
-    while spent < budget_s and len(pick) < len(order):
-        new = [int(x) for x in order[len(pick)::max(1, len(order) // 8)][:n]]
-        new = [s for s in new if s not in pick] or [int(order[len(pick)])]
-        smp = oracle_sample(wl, sorted(new))
-        t0 = time.perf_counter()
-        oracle_pass(smp)
-        dt = time.perf_counter() - t0
-        spent += dt
-        total_bytes += sample_bytes(wl, smp)
-        pick.extend(new)
-        n *= 2
-    return {"value": total_bytes / spent / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
-            "kind": "oracle",
-            "sample": f"{len(pick)} of {wl.num_seqs} sequences (all heads) of {wl.name}: "
-                      f"fp64 KV write + attention, {spent:.1f} s of CPU"}
+    spent, nbytes, passes = 0.0, 0, 0
+    while spent < budget_s:
+        for smp in samples:
+            t0 = time.perf_counter()
+            oracle_pass(smp)
+            spent += time.perf_counter() - t0
+            nbytes += sample_bytes(smp)
+        passes += 1
+    return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(samples)} of {num_seqs} sequences (all heads) of {name}, "
+                      f"{passes} passes: fp64 KV write + attention per sequence, "
+                      f"{spent:.1f} s wall on the host cores"}
 
 
 # ----------------------------------------------------------------- arms
@@ -230,7 +233,10 @@ def run_pkv(args, rank, world, device):
 
     build.build()
     pkv.load()
-    wl = W.workload(args.workload, device=device, seed=W.SEED_BASE + args.workload + 1000 * rank)
+    wl = W.workload(args.workload, device=device, seed=W.SEED_BASE + args.workload + 1000 * rank,
+                    num_seqs=args.num_seqs)
+    if args.profile:
+        return profile_only(args, wl)
     attn_b, write_b, kv_b = algorithmic_bytes(wl)
     step_b = attn_b + write_b
     out = torch.empty_like(wl.q)
@@ -240,10 +246,15 @@ def run_pkv(args, rank, world, device):
     ws_n = pkv.workspace_size(wl.k_cache, meta)
     ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    max_splits = 0
-    if ws_n:
-        max_splits = 1  # combine launched
-    launches_per_step = 1 + 1 + (1 if ws_n else 0) + (1 if wl.num_decode_seqs < wl.num_seqs else 0)
+    nd = wl.num_seqs if wl.max_query_len <= 1 else wl.num_decode_seqs
+    launches_per_step = (1 + (1 if nd > 0 else 0) + (1 if ws_n else 0)
+                         + (1 if nd < wl.num_seqs else 0))
+    # Oracle inputs are copied from the pristine (pre-step) cache.
+    spot = oracle_sample(wl, [int(np.argmin(wl.ctx_lens)), int(np.argmax(wl.ctx_lens))])
+    base_samples = []
+    if rank == 0 and not args.no_cpu_baseline:
+        perm = np.random.default_rng(0).permutation(wl.num_seqs)[:12]
+        base_samples = [oracle_sample(wl, [int(s)]) for s in perm]
 
     def step():
         pkv.run_step(wl, out, workspace=ws, kv_split_tokens=args.kv_split, stream=stream)
@@ -287,7 +298,7 @@ def run_pkv(args, rank, world, device):
     if pkv.get_error(clear=True):
         raise RuntimeError("device error word set during the timed region")
     # parity spot check on the timed output: a few rows against the oracle
-    parity = spot_check(wl, out)
+    parity = spot_check(wl, out, spot)
 
     t = torch.tensor([total_ms], device=device)
     if world > 1:
@@ -345,25 +356,32 @@ def run_pkv(args, rank, world, device):
         "e2e": e2e,
         "parity_max_abs_err": parity,
     }
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+    if base_samples:
+        line["cpu_baseline"] = cpu_baseline(base_samples, wl.name, wl.num_seqs)
     return line
 
 
-def spot_check(wl, out):
-    """Max |error| of a few timed output rows against the oracle."""
-    import oracle
-    seqs = [int(np.argmin(wl.ctx_lens)), int(np.argmax(wl.ctx_lens))]
-    # the cache already holds this step's tokens; rebuild the sample from the
-    # pre-write view by letting the oracle rewrite the same rows (idempotent)
-    smp = oracle_sample(wl, seqs)
-    exp = oracle_pass(smp)
-    rows = []
-    qsl = wl.query_start_loc.cpu().numpy()
-    for s in seqs:
-        rows.extend(range(int(qsl[s]), int(qsl[s + 1])))
-    got = out[torch.tensor(rows, device=out.device)].float().cpu().numpy().astype(np.float64)
-    err = float(np.abs(got - exp).max())
+def profile_only(args, wl):
+    """Warm-up then `steps` plain steps, nothing else: a short, fixed launch
+    sequence for ncu captures (not a bench measurement)."""
+    from paged_kv_cache_43_gb300 import pkv
+    out = torch.empty_like(wl.q)
+    for _ in range(args.warmup + args.steps):
+        pkv.run_step(wl, out, kv_split_tokens=args.kv_split)
+    torch.cuda.synchronize()
+    if pkv.get_error(clear=True):
+        raise RuntimeError("device error word set")
+    print(json.dumps({"profile_run": wl.name, "num_seqs": wl.num_seqs,
+                      "steps": args.warmup + args.steps}), flush=True)
+    return None
+
+
+def spot_check(wl, out, spot):
+    """Max |error| of the timed output rows of the spot sample against the
+    oracle (run on the pre-step copy)."""
+    exp = oracle_pass(spot)
+    got = out[torch.tensor(spot["rows"], device=out.device)].float().cpu().numpy()
+    err = float(np.abs(got.astype(np.float64) - exp).max())
     if not (err <= (2e-2 if wl.dtype == torch.bfloat16 else 1e-5)):
         raise RuntimeError(f"timed output fails parity: max abs err {err}")
     return err
@@ -383,6 +401,9 @@ def end_to_end(wl, args, stream, device, step_bytes):
     d2h = out_h.numel() * out_h.element_size()
     meta_kw = dict(max_query_len=wl.max_query_len, max_context_len=wl.max_context_len,
                    num_decode_seqs=wl.num_decode_seqs, kv_split_tokens=args.kv_split)
+    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **meta_kw)
+    ws = torch.empty(max(pkv.workspace_size(wl.k_cache, meta), 1), dtype=torch.uint8,
+                     device=device)
 
     def e2e_step():
         with torch.cuda.stream(stream):
@@ -392,7 +413,7 @@ def end_to_end(wl, args, stream, device, step_bytes):
                   stream=stream)
         pkv.attention(out_d, dev["q"], wl.k_cache, wl.v_cache, dev["block_tables"],
                       dev["context_lens"], dev["query_start_loc"], wl.scale, stream=stream,
-                      **meta_kw)
+                      workspace=ws, **meta_kw)
         with torch.cuda.stream(stream):
             out_h.copy_(out_d, non_blocking=True)
 
@@ -416,7 +437,8 @@ def end_to_end(wl, args, stream, device, step_bytes):
 def run_reference(args, rank, world):
     """The oracle as the reference arm: each step is the oracle's KV write +
     attention on a bounded sample of the same workload (generated on the GPU
-    with the same seed, copied to the host)."""
+    with the same seed, copied to the host), sized so that warm-up + steps
+    take about PKV_REFERENCE_BUDGET_S seconds (default 150)."""
     if rank != 0:
         return None
     from paged_kv_cache_43_gb300 import workloads as W
@@ -424,43 +446,35 @@ def run_reference(args, rank, world):
     oracle.build()
     device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     wl = W.workload(args.workload, device=device)
-    attn_b, write_b, _ = algorithmic_bytes(wl)
-    # pick the sample so that warmup + steps fit in about budget seconds
     budget = float(os.environ.get("PKV_REFERENCE_BUDGET_S", "150"))
-    order = [int(x) for x in np.argsort(wl.ctx_lens)]
-    smp = oracle_sample(wl, [order[len(order) // 2]])
+    seq = int(np.argsort(wl.ctx_lens)[wl.num_seqs // 2])      # median-length sequence
+    smp = oracle_sample(wl, [seq])
     t0 = time.perf_counter()
     oracle_pass(smp)
     one = time.perf_counter() - t0
     per_step = budget / max(args.steps + args.warmup, 1)
+    hkv = wl.num_kv_heads
     if one > per_step:
-        # shrink to a head subset of one sequence
-        frac = max(per_step / one, 1.0 / wl.num_q_heads)
-        smp["q"] = smp["q"][:, : max(1, int(wl.num_q_heads * frac)) // (wl.num_q_heads // wl.num_kv_heads) * (wl.num_q_heads // wl.num_kv_heads) or (wl.num_q_heads // wl.num_kv_heads)]
+        hkv = max(1, int(wl.num_kv_heads * per_step / one))
+        smp = oracle_sample(wl, [seq], kv_heads=hkv)
     for _ in range(args.warmup):
         oracle_pass(smp)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle_pass(smp)
     dt = time.perf_counter() - t0
-    hq_used = smp["q"].shape[1]
-    e = wl.q.element_size()
-    keys = int(smp["cl"].sum())
-    t = int(smp["qsl"][-1])
-    g = wl.num_q_heads // wl.num_kv_heads
-    hkv_used = max(1, hq_used // g)
-    b = keys * hkv_used * wl.head_size * e * 2 + 2 * t * hq_used * wl.head_size * e
-    value = b * args.steps / dt / 1e9
-    ms = dt / args.steps * 1e3
+    value = sample_bytes(smp) * args.steps / dt / 1e9
+    sample = (f"sequence {seq} of {wl.name} ({int(smp['cl'][0])} keys), {hkv} of "
+              f"{wl.num_kv_heads} kv heads with their q heads, fp64 KV write + attention")
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same seeded workload, bounded sample)", "impl": "reference",
-        "config": {"workload": wl.name, "sample": f"1 sequence ({keys} keys), {hq_used} of "
-                   f"{wl.num_q_heads} q heads per step"},
+        "config": {"workload": wl.name, "sample": sample},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
-                         "kind": "oracle", "sample": f"1 sequence of {wl.name}, {hq_used} heads"},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -475,6 +489,10 @@ def main():
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--kv-split", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="override the batch size (profiling captures on a smaller case)")
+    ap.add_argument("--profile", action="store_true",
+                    help="run warmup+steps plain steps only (for ncu), print no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

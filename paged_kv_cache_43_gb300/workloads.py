@@ -197,18 +197,22 @@ def _log_uniform_int(rng, lo, hi, n):
     return np.floor(np.exp(rng.uniform(np.log(lo), np.log(hi), size=n))).astype(np.int64)
 
 
-def lengths(n: int, small: bool = False, seed: int | None = None):
+def lengths(n: int, small: bool = False, seed: int | None = None, num_seqs: int | None = None):
     """(q_lens, ctx_lens, extra kwargs) of workload n.  ``small`` keeps the head
     layout but shrinks batch and context so that the oracle finishes in seconds
-    while the kernels still see several tiles, splits and ragged tails."""
+    while the kernels still see several tiles, splits and ragged tails.
+    ``num_seqs`` overrides the batch size of the decode workloads 2, 3 and 5
+    (same length distribution)."""
     rng = np.random.default_rng(SEED_BASE + n if seed is None else seed)
     if n == 1:
         return np.ones(4, np.int64), np.array([17, 33, 64, 100]), {}
     if n == 2:
         S, hi = (6, 1200) if small else (64, 4096)
+        S = num_seqs or S
         return np.ones(S, np.int64), _uniform_int(rng, 128, hi, S), {}
     if n == 3:
         S, hi = (24, 2048) if small else (256, 8192)
+        S = num_seqs or S
         return np.ones(S, np.int64), _log_uniform_int(rng, 64, hi, S), {}
     if n == 4:
         if small:
@@ -223,6 +227,7 @@ def lengths(n: int, small: bool = False, seed: int | None = None):
         return q, ctx, dict(shared_prefix_blocks=shb, shared_seqs=tuple(range(nsh)))
     if n == 5:
         S, lo, hi = (2, 3000, 6000) if small else (16, 16384, 32768)
+        S = num_seqs or S
         return np.ones(S, np.int64), _uniform_int(rng, lo, hi, S), {}
     raise ValueError(n)
 
@@ -231,10 +236,10 @@ HEADS = {1: (4, 4, 64), 2: (32, 32, 128), 3: (32, 8, 128), 4: (32, 8, 128), 5: (
 
 
 def workload(n: int, *, small: bool = False, device="cpu", poison=True,
-             seed: int | None = None) -> Workload:
+             seed: int | None = None, num_seqs: int | None = None) -> Workload:
     """Workload n (1..5) at full size, or its small parity variant."""
     seed = SEED_BASE + n if seed is None else seed
-    q_lens, ctx, extra = lengths(n, small=small, seed=seed)
+    q_lens, ctx, extra = lengths(n, small=small, seed=seed, num_seqs=num_seqs)
     hq, hkv, d = HEADS[n]
     kw = dict(num_q_heads=hq, num_kv_heads=hkv, head_size=d, seed=seed, device=device,
               poison=poison, name=WORKLOAD_NAMES[n] + ("-small" if small else ""), **extra)
