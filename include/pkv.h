@@ -157,6 +157,42 @@ int pkv_attention(void *out, const void *q, const void *k_cache,
                   const pkv_attn_meta *meta, void *workspace,
                   size_t workspace_bytes, void *stream);
 
+/* Bytes of the fixed scratch array behind pkv_attention_static_scratch. */
+#define PKV_STATIC_SCRATCH_BYTES (64u << 20) /* 64 MiB per GPU */
+
+/* pkv_attention for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this call; it exists for users of this library.
+ *
+ * Who needs it: a caller that has no way to hand pkv_attention a workspace,
+ * such as a plugin inside a host framework that owns every device
+ * allocation through its own pool (a stray cudaMalloc there can synchronise
+ * the device and escapes the pool's accounting), or a decode loop that must
+ * never enter the allocator.
+ *
+ * What it does: exactly pkv_attention (same arguments, same results), with
+ * the split-K workspace taken from a fixed array of PKV_STATIC_SCRATCH_BYTES
+ * inside the library instead of from the caller.  Every GPU on which the
+ * library's device code is loaded holds that array until the process exits.
+ * The call itself allocates nothing and frees nothing.
+ *
+ * Limits and sharing:
+ *   - A batch whose workspace (pkv_attention_workspace_size) exceeds
+ *     PKV_STATIC_SCRATCH_BYTES is rejected with PKV_E_WORKSPACE before
+ *     anything is enqueued; a larger kv_split_tokens shrinks the need.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; nothing in it has to start at zero (each call writes every
+ *     partial it reads).  Calls whose GPU work overlaps (e.g. on two streams
+ *     without ordering) race on the array: order them.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture. */
+int pkv_attention_static_scratch(void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens,
+                                 const int32_t *query_start_loc, float scale,
+                                 const pkv_cache_desc *cache,
+                                 const pkv_attn_meta *meta, void *stream);
+
 /* Reads (and, if clear != 0, resets) the current device's error word: the OR
  * of PKV_ERR_* bits raised by kernels since the last clear.  SYNCHRONISES the
  * device first.  Returns PKV_OK or PKV_E_CUDA. */

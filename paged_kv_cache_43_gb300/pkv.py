@@ -24,7 +24,8 @@ ERR_QUERY_LEN = 1 << 3
 ERR_DECODE_QLEN = 1 << 4
 ERR_TIMEOUT = 1 << 5
 EXPORTED = ("pkv_write", "pkv_attention_workspace_size", "pkv_attention",
-            "pkv_get_error", "pkv_status_string")
+            "pkv_attention_static_scratch", "pkv_get_error", "pkv_status_string")
+STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class PkvError(RuntimeError):
@@ -69,6 +70,10 @@ def load(path: str | None = None):
         lib.pkv_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                       ctypes.POINTER(CacheDesc), ctypes.POINTER(AttnMeta),
                                       vp, ctypes.c_size_t, vp]
+        lib.pkv_attention_static_scratch.restype = ctypes.c_int
+        lib.pkv_attention_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                                     ctypes.POINTER(CacheDesc),
+                                                     ctypes.POINTER(AttnMeta), vp]
         lib.pkv_get_error.restype = ctypes.c_int
         lib.pkv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -168,6 +173,29 @@ def attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start_
                              context_lens.data_ptr(), query_start_loc.data_ptr(),
                              float(scale), ctypes.byref(desc), ctypes.byref(meta),
                              ws_ptr, ws_bytes, _stream(stream)))
+
+
+def attention_static_scratch(out, q, k_cache, v_cache, block_tables, context_lens,
+                             query_start_loc, scale, *, max_query_len, max_context_len,
+                             num_decode_seqs=-1, kv_split_tokens=0, stream=None) -> int:
+    """pkv_attention_static_scratch: pkv_attention with the split-K workspace
+    taken from the library's own fixed device array (no allocation anywhere).
+    Returns the C status (0 = enqueued; PKV_E_WORKSPACE = batch needs more than
+    STATIC_SCRATCH_BYTES)."""
+    lib = load()
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n, dtype=k_cache.dtype)
+    _require(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _require(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    _require(query_start_loc, "query_start_loc", dtype=torch.int32, ndim=1)
+    meta = attn_meta(q, block_tables, context_lens, max_query_len=max_query_len,
+                     max_context_len=max_context_len, num_decode_seqs=num_decode_seqs,
+                     kv_split_tokens=kv_split_tokens)
+    desc = cache_desc(k_cache)
+    return int(lib.pkv_attention_static_scratch(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), context_lens.data_ptr(), query_start_loc.data_ptr(),
+        float(scale), ctypes.byref(desc), ctypes.byref(meta), _stream(stream)))
 
 
 def get_error(clear: bool = True) -> int:
