@@ -19,8 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libpkv.so")
-SOURCES = ["pkv_api.cu", "pkv_write.cu", "pkv_decode.cu", "pkv_prefill.cu", "pkv_f32.cu",
-           "pkv_static_scratch.cu"]
+SOURCES = ["pkv_api.cu", "pkv_write.cu", "pkv_decode.cu", "pkv_prefill.cu", "pkv_prefill_tc.cu",
+           "pkv_f32.cu", "pkv_static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

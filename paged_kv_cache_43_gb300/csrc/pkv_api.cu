@@ -78,6 +78,27 @@ int encode_cache_map(CUtensorMap* map, const void* base, const pkv_cache_desc& c
   return r == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
 }
 
+// TMA descriptor of the bf16 query tensor [num_tokens, num_q_heads, D] viewed
+// as (D, Hq, T) with a box of 64 columns x `group` heads x 128/group tokens:
+// one box is the 128-row (token, head) tile of one kv head, 128 bytes wide.
+int encode_query_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads,
+                     int head_size, int group) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn;
+  if (int st = encode_fn(&fn)) return st;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_size),
+                              static_cast<cuuint64_t>(num_q_heads),
+                              static_cast<cuuint64_t>(num_tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_size) * 2,
+                                 static_cast<cuuint64_t>(num_q_heads) * head_size * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group),
+                             static_cast<cuuint32_t>(prefill_tc_tokens_per_cta(group))};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_cache(const pkv_cache_desc* c) {
@@ -284,12 +305,26 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
     f.num_kv_heads = cache->num_kv_heads;
     f.group = G;
     f.num_blocks = cache->num_blocks;
-    const int64_t rows = static_cast<int64_t>(meta->max_query_len) * G;
-    f.num_mtiles = static_cast<int32_t>((rows + kPrefillRows - 1) / kPrefillRows);
     f.num_tokens = meta->num_tokens;
     f.max_query_len = meta->max_query_len;
     f.scale_log2 = scale * LOG2E;
-    if (launch_prefill_bf16(kmap, vmap, f, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
+    if (prefill_tc_supported(cache->head_size, G)) {
+      // tcgen05/TMEM kernel: 128/G tokens x G heads per CTA.
+      const int toks = prefill_tc_tokens_per_cta(G);
+      f.num_mtiles = (meta->max_query_len + toks - 1) / toks;
+      CUtensorMap qmap;
+      if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
+                                   cache->head_size, G))
+        return e;
+      if (launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, st) != cudaSuccess)
+        return PKV_E_CUDA;
+    } else {
+      // Group sizes that do not divide 128 rows: mma.sync kernel, 64 rows per CTA.
+      const int64_t rows = static_cast<int64_t>(meta->max_query_len) * G;
+      f.num_mtiles = static_cast<int32_t>((rows + kPrefillRows - 1) / kPrefillRows);
+      if (launch_prefill_bf16(kmap, vmap, f, cache->head_size, st) != cudaSuccess)
+        return PKV_E_CUDA;
+    }
   }
   return PKV_OK;
 }

@@ -102,8 +102,10 @@ def test_decode_edge_lengths_and_groups(hq, hkv, d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (32, 8), (3, 1)])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (32, 8), (3, 1), (16, 1), (64, 8), (6, 2),
+                                    (128, 1)])
 def test_prefill_edge_chunks(hq, hkv, d):
+    """Group sizes dividing 128 run the tcgen05 kernel, others (3) the mma.sync one."""
     q_lens = [1, 5, 16, 63, 64, 65, 97, 1, 40]
     ctx = [1, 5, 40, 63, 130, 65, 97, 2, 200]   # includes whole-prompt chunks
     wl = W.make_workload(q_lens, ctx, num_q_heads=hq, num_kv_heads=hkv, head_size=d,
