@@ -91,7 +91,7 @@ int encode_query_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_size) * 2,
                                  static_cast<cuuint64_t>(num_q_heads) * head_size * 2};
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group),
-                             static_cast<cuuint32_t>(prefill_tc_tokens_per_cta(group))};
+                             static_cast<cuuint32_t>(prefill_tc_tokens_per_tile(group))};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -309,7 +309,7 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
     f.max_query_len = meta->max_query_len;
     f.scale_log2 = scale * LOG2E;
     if (prefill_tc_supported(cache->head_size, G)) {
-      // tcgen05/TMEM kernel: 128/G tokens x G heads per CTA.
+      // tcgen05/TMEM kernel: two tiles of 128/G tokens x G heads per CTA.
       const int toks = prefill_tc_tokens_per_cta(G);
       f.num_mtiles = (meta->max_query_len + toks - 1) / toks;
       CUtensorMap qmap;

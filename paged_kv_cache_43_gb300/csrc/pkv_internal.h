@@ -97,8 +97,10 @@ cudaError_t launch_prefill_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap
                                 const PrefillArgs& a, int head_size, cudaStream_t stream);
 cudaError_t launch_attention_f32(const F32Args& a, cudaStream_t stream);
 
-// tcgen05 prefill: 128 rows = (128 / group) tokens x group heads per CTA.
+// tcgen05 prefill: query tiles of 128 rows = (128 / group) tokens x group heads,
+// two tiles per CTA.
 bool prefill_tc_supported(int head_size, int group);
+int prefill_tc_tokens_per_tile(int group);
 int prefill_tc_tokens_per_cta(int group);
 cudaError_t launch_prefill_tc(const CUtensorMap& qmap, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const PrefillArgs& a, int head_size,

@@ -9,21 +9,25 @@
 // non-cascadé").  GQA: the G query heads of a kv head share every K/V tile.
 //
 // GB300 design (the dense contraction of the path):
-//  * CTA = 128 rows x one kv head of one sequence; a row is a (token, q head)
-//    pair with the head fastest, so 128/G tokens x G heads.  The Q tile is one
-//    TMA load per 64-column half (box 64 x G heads x 128/G tokens, 128-byte
-//    swizzle), which lands exactly in the K-major UMMA layout.
+//  * CTA = two 128-row query tiles x one kv head of one sequence (one CTA per
+//    SM); a row is a (token, q head) pair with the head fastest, so each tile
+//    holds 128/G tokens x G heads and is one TMA load per 64-column half
+//    (box 64 x G heads x 128/G tokens, 128-byte swizzle), which lands exactly
+//    in the K-major UMMA layout.
 //  * warp 0 streams 64-key K/V tiles (4 cache blocks, one TMA box per block
-//    and half) into a 2-stage ring; warp 1 allocates 256 TMEM columns and one
-//    of its threads issues every MMA:
-//        S  = Q K^T   (M=128, N=64,  K=16 x D/16, both operands from smem)
-//        O += P V     (M=128, N=D,   K=16 x 4, P from TMEM, V MN-major smem)
-//    S of tile j+1 is computed while the softmax works on tile j.
-//  * warps 2-5 own one TMEM lane (= one row) per thread: they load a row of S,
-//    apply the causal mask, keep a lazily updated running max (O is rescaled in
-//    TMEM only when the max grows by more than 2^8), write P (bf16) back to
-//    TMEM for the second MMA, and at the end read O, divide by the row sum and
-//    store bf16.  No shuffles: a thread holds its whole row.
+//    and half) into a 4-stage ring shared by both query tiles; warp 1
+//    allocates all 512 TMEM columns and one of its threads issues every MMA:
+//        S_t  = Q_t K^T   (M=128, N=64, K=16 x D/16, operands from smem)
+//        O_t += P_t V     (M=128, N=D,  K=16 x 4, P_t from TMEM, V MN-major)
+//    for the two tiles t in turn, so the tensor core works on one tile while
+//    the softmax of the other runs, and S_t of the next K/V tile is computed
+//    as soon as the softmax has read the current one.
+//  * warps 2-5 and 6-9 (one warpgroup per query tile) own one TMEM lane
+//    (= one row) per thread: they load a row of S, apply the causal mask, keep
+//    a lazily updated running max (O is rescaled in TMEM only when the max
+//    grows by more than 2^8), write P (bf16) to TMEM for the second MMA, and at
+//    the end read O, divide by the row sum and store bf16.  No shuffles: a
+//    thread holds its whole row.
 //  * every wait is an mbarrier with a bounded spin and a CTA-wide abort flag;
 //    TMEM is freed on every path.
 #include "pkv_common.cuh"
@@ -34,26 +38,31 @@ namespace pkv {
 
 namespace {
 
-constexpr int kTcRows = 128;      // UMMA M
+constexpr int kTcRows = 128;      // UMMA M (rows of one query tile)
+constexpr int kTcTiles = 2;       // query tiles per CTA
 constexpr int kTcKeys = 64;       // keys per K/V tile
-constexpr int kTcThreads = 192;   // 6 warps
-constexpr int kTcStages = 2;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColP = 64, kColO = 128;
+constexpr int kTcThreads = 320;   // load, MMA, 2 x 4 softmax warps
+constexpr int kTcStages = 4;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: S of tile t at 64t, P of tile t at 128 + 32t, O of tile t at 256 + 128t.
+__host__ __device__ constexpr uint32_t col_s(int t) { return 64u * t; }
+__host__ __device__ constexpr uint32_t col_p(int t) { return 128u + 32u * t; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
 constexpr float kLazyRescale = 8.0f;  // log2 units: rescale O only past 2^8 growth
 
 template <int D>
 struct TcLayout {
   static constexpr int kHalves = D / 64;
   static constexpr int kQHalf = kTcRows * 128;       // 16 KB: 128 rows x 128 B
-  static constexpr int kQBytes = kHalves * kQHalf;
+  static constexpr int kQTile = kHalves * kQHalf;
   static constexpr int kKvHalf = kTcKeys * 128;      // 8 KB: 64 keys x 128 B
   static constexpr int kKBytes = kHalves * kKvHalf;
   static constexpr int kStageBytes = 2 * kKBytes;    // K then V
 };
 
 struct TcShared {
-  uint64_t q_full, s_full, s_free, p_full, pv_done, drain;
+  uint64_t q_full, drain;
+  uint64_t s_full[kTcTiles], s_free[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
   uint64_t kv_full[kTcStages], kv_empty[kTcStages];
   uint32_t tmem_base;
   int32_t abort;
@@ -61,21 +70,21 @@ struct TcShared {
 
 template <int D>
 constexpr int tc_smem_bytes() {
-  // Padded so that at most two CTAs (2 x 256 TMEM columns) share an SM.
-  constexpr int need = 1024 + TcLayout<D>::kQBytes + kTcStages * TcLayout<D>::kStageBytes +
-                       static_cast<int>(sizeof(TcShared));
-  return need > 80 * 1024 ? need : 80 * 1024;
+  // Whole-SM footprint: one CTA per SM (it owns all 512 TMEM columns).
+  constexpr int need = 1024 + kTcTiles * TcLayout<D>::kQTile +
+                       kTcStages * TcLayout<D>::kStageBytes + static_cast<int>(sizeof(TcShared));
+  return need > 120 * 1024 ? need : 120 * 1024;
 }
 
 // Bounded wait that also gives up when another thread of the CTA has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int32_t* abort, int32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_test(bar, parity)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
@@ -97,8 +106,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, 1)
     pkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -106,8 +121,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sKV = smem + Lt::kQBytes;
+  uint8_t* sQ = smem;                                   // [tile][half][128 rows x 128 B]
+  uint8_t* sKV = smem + kTcTiles * Lt::kQTile;          // [stage][K halves | V halves]
   TcShared* sh = reinterpret_cast<TcShared*>(sKV + kTcStages * Lt::kStageBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -117,7 +132,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int mtile = a.num_mtiles - 1 - blockIdx.x;  // heaviest first
   const int G = a.group;
   const int Hq = a.num_q_heads;
-  const int toks = kTcRows / G;                     // tokens per CTA
+  const int tile_toks = kTcRows / G;                // tokens per query tile
+  const int toks = kTcTiles * tile_toks;            // tokens per CTA
 
   const int L = __ldg(a.context_lens + s);
   const int q0 = __ldg(a.query_start_loc + s);
@@ -143,23 +159,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     return;
   }
   const int tok_last = min(tok0 + toks, qn) - 1;
+  const int ntq = (tok0 + tile_toks < qn) ? 2 : 1;  // query tiles holding a valid row
   const int pos_max = L - qn + tok_last;            // last key any row here can see
   const int ntiles = (pos_max + kTcKeys) / kTcKeys;
   const int nblk = (pos_max + kBlock) / kBlock;
 
-  const uint32_t q_full = smem_u32(&sh->q_full), s_full = smem_u32(&sh->s_full);
-  const uint32_t s_free = smem_u32(&sh->s_free), p_full = smem_u32(&sh->p_full);
-  const uint32_t pv_done = smem_u32(&sh->pv_done), drain = smem_u32(&sh->drain);
+  const uint32_t q_full = smem_u32(&sh->q_full), drain = smem_u32(&sh->drain);
   if (threadIdx.x == 0) {
     prefetch_tensor_map(&qmap);
     prefetch_tensor_map(&kmap);
     prefetch_tensor_map(&vmap);
     mbar_init(q_full, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 4);
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
+    for (int t = 0; t < kTcTiles; ++t) {
+      mbar_init(smem_u32(&sh->s_full[t]), 1);
+      mbar_init(smem_u32(&sh->s_free[t]), 4);
+      mbar_init(smem_u32(&sh->p_full[t]), 4);
+      mbar_init(smem_u32(&sh->pv_done[t]), 1);
+    }
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(smem_u32(&sh->kv_full[i]), 1);
       mbar_init(smem_u32(&sh->kv_empty[i]), 1);
@@ -179,11 +196,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const uint64_t keep = policy_evict_normal();   // K/V tiles are re-read by the
     const int32_t* bt = a.block_tables + static_cast<int64_t>(s) * a.bt_stride;  // other row tiles
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, Lt::kQBytes);
+      mbar_arrive_expect_tx(q_full, ntq * Lt::kQTile);
+      for (int t = 0; t < ntq; ++t)
 #pragma unroll
-      for (int h = 0; h < Lt::kHalves; ++h)
-        tma_load_3d(smem_u32(sQ + h * Lt::kQHalf), &qmap, q_full, h * 64, kvh * G, q0 + tok0,
-                    keep);
+        for (int h = 0; h < Lt::kHalves; ++h)
+          tma_load_3d(smem_u32(sQ + t * Lt::kQTile + h * Lt::kQHalf), &qmap, q_full, h * 64,
+                      kvh * G, q0 + tok0 + t * tile_toks, keep);
     }
     int my_bid = -1;
     for (int it = 0; it < ntiles; ++it) {
@@ -232,9 +250,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kTcKeys, 0, 0);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
-      const uint32_t tS = tmem + kColS, tP = tmem + kColP, tO = tmem + kColO;
-      const uint32_t q_addr = smem_u32(sQ);
-      auto issue_s = [&](int j) {
+      auto issue_s = [&](int t, int j) {
+        const uint32_t q_addr = smem_u32(sQ + t * Lt::kQTile);
         const uint32_t k_addr = smem_u32(sKV + (j % kTcStages) * Lt::kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -243,36 +260,71 @@ __global__ void __launch_bounds__(kTcThreads, 2)
               tc::smem_desc_sw128(q_addr + (kk >> 2) * Lt::kQHalf + off, 16, 1024);
           const uint64_t db =
               tc::smem_desc_sw128(k_addr + (kk >> 2) * Lt::kKvHalf + off, 16, 1024);
-          tc::mma_ss(tS, da, db, idS, kk > 0 ? 1u : 0u);
+          tc::mma_ss(tmem + col_s(t), da, db, idS, kk > 0 ? 1u : 0u);
         }
-        tc::commit(s_full);
+        tc::commit(smem_u32(&sh->s_full[t]));
       };
-      bool ok = wait_or_abort(q_full, 0, abort, a.err) &&
-                wait_or_abort(smem_u32(&sh->kv_full[0]), 0, abort, a.err);
-      if (ok) {
-        tc::fence_after_sync();
-        issue_s(0);
-      }
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (j + 1 < ntiles) {
-          const int jn = j + 1;
-          ok = wait_or_abort(smem_u32(&sh->kv_full[jn % kTcStages]), (jn / kTcStages) & 1,
-                             abort, a.err) &&
-               wait_or_abort(s_free, j & 1, abort, a.err);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_s(jn);
-        }
-        if (!(ok = wait_or_abort(p_full, j & 1, abort, a.err))) break;
-        tc::fence_after_sync();
-        const uint32_t v_addr = smem_u32(sKV + (j % kTcStages) * Lt::kStageBytes + Lt::kKBytes);
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t v_addr =
+            smem_u32(sKV + (j % kTcStages) * Lt::kStageBytes + Lt::kKBytes);
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks) {
           const uint64_t dv = tc::smem_desc_sw128(v_addr + ks * 2048, Lt::kKvHalf, 1024);
-          tc::mma_ts(tO, tP + ks * 8, dv, idO, (j > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_ts(tmem + col_o(t), tmem + col_p(t) + ks * 8, dv, idO,
+                     (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc::commit(pv_done);
-        tc::commit(smem_u32(&sh->kv_empty[j % kTcStages]));
+        tc::commit(smem_u32(&sh->pv_done[t]));
+      };
+      // Event loop: issue whichever MMA is ready, never blocking on one
+      // tile while the other could use the tensor core.  Phases cannot run
+      // more than one ahead of what this thread has seen, so parity probes
+      // are unambiguous.
+      int s_next[kTcTiles] = {0, 0};   // next tile index whose S is issued
+      int pv_next[kTcTiles] = {0, 0};  // next tile index whose P V is issued
+      int released = 0;                // K/V stages handed back to the producer
+      bool ok = wait_or_abort(q_full, 0, abort, a.err);
+      uint64_t idle_since = 0;
+      while (ok) {
+        bool progress = false;
+        for (int t = 0; t < ntq; ++t) {
+          const int js = s_next[t];
+          if (js < ntiles &&
+              mbar_test(smem_u32(&sh->kv_full[js % kTcStages]), (js / kTcStages) & 1) &&
+              (js == 0 || mbar_test(smem_u32(&sh->s_free[t]), (js - 1) & 1))) {
+            tc::fence_after_sync();
+            issue_s(t, js);
+            s_next[t] = js + 1;
+            progress = true;
+          }
+          const int jp = pv_next[t];
+          if (jp < s_next[t] && mbar_test(smem_u32(&sh->p_full[t]), jp & 1)) {
+            tc::fence_after_sync();
+            issue_pv(t, jp);
+            pv_next[t] = jp + 1;
+            progress = true;
+          }
+        }
+        int done_pv = pv_next[0];
+        if (ntq > 1) done_pv = min(done_pv, pv_next[1]);
+        while (released < done_pv) {  // every P V of that stage is issued
+          tc::commit(smem_u32(&sh->kv_empty[released % kTcStages]));
+          ++released;
+        }
+        if (done_pv == ntiles) break;
+        if (progress) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = global_timer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (*abort) {
+            ok = false;
+          } else if (now - idle_since > kWaitLimitNs) {
+            *abort = 1;
+            raise_error(a.err, PKV_ERR_TIMEOUT);
+            ok = false;
+          }
+        }
       }
       // Every MMA issued here must finish before TMEM is released.
       tc::commit(drain);
@@ -281,74 +333,97 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    const int t = (warp - 2) >> 2;                // query tile of this warpgroup
     const int quarter = warp & 3;                 // TMEM lanes this warp may touch
     const int row = quarter * 32 + lane;          // tile row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int tok = tok0 + row / G;
+    const int tok = tok0 + t * tile_toks + row / G;
     const int g = row % G;
     const bool valid = tok <= tok_last;
     const int pos = L - qn + (valid ? tok : tok_last);
-    const int ts = (warp - 2) * 32 + lane;        // 0..127 among softmax threads
+    const int ts = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the warpgroup
+    const uint32_t b_sfull = smem_u32(&sh->s_full[t]), b_sfree = smem_u32(&sh->s_free[t]);
+    const uint32_t b_pfull = smem_u32(&sh->p_full[t]), b_pvdone = smem_u32(&sh->pv_done[t]);
+    const uint32_t tS = tmem + lane_off + col_s(t), tP = tmem + lane_off + col_p(t);
+    const uint32_t tO = tmem + lane_off + col_o(t);
+    const float sl2 = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
-    bool done = true;
-    for (int j = 0; j < ntiles; ++j) {
-      if (!warp_wait(s_full, j & 1, abort, a.err)) { done = false; break; }
+    bool done = t < ntq;
+    for (int j = 0; done && j < ntiles; ++j) {
+      if (!warp_wait(b_sfull, j & 1, abort, a.err)) { done = false; break; }
       tc::fence_after_sync();
       uint32_t sr[2][32];
-      tc::ld32(tmem + lane_off + kColS, sr[0]);
-      tc::ld32(tmem + lane_off + kColS + 32, sr[1]);
+      tc::ld32(tS, sr[0]);
+      tc::ld32(tS + 32, sr[1]);
       tc::wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      // scores in the log2 domain, causal mask (also hides keys >= L)
+      if (lane == 0) mbar_arrive(b_sfree);
+      // causal mask on raw scores (also hides keys >= L); scale > 0, so the
+      // row max of the raw scores gives the max of the scaled ones
       const int key0 = j * kTcKeys;
-      const bool need_mask = key0 + kTcKeys - 1 > pos;
-      float mt = -INFINITY;
+      float x[kTcKeys];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int c = 0; c < kTcKeys; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+      if (key0 + kTcKeys - 1 > pos) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float x = __uint_as_float(sr[h][c]) * a.scale_log2;
-          if (need_mask && key0 + h * 32 + c > pos) x = -INFINITY;
-          sr[h][c] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
-        }
+        for (int c = 0; c < kTcKeys; ++c) x[c] = (key0 + c > pos) ? -INFINITY : x[c];
+      }
+      // row max: four independent chains of three-input maxima
+      float m4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+      for (int c = 4; c < kTcKeys; c += 8) {
+        m4[0] = tc::max3(m4[0], x[c], x[c + 1]);
+        m4[1] = tc::max3(m4[1], x[c + 2], x[c + 3]);
+        m4[2] = tc::max3(m4[2], x[c + 4], x[c + 5]);
+        m4[3] = tc::max3(m4[3], x[c + 6], x[c + 7]);
+      }
+      const float mt = tc::max3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
       float alpha = 1.f;
       if (mt > m_used + kLazyRescale) {
-        alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - mt);
+        alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - mt);
         m_used = mt;
       }
-      const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+      const float neg_mu = (m_used == -INFINITY) ? 0.f : -m_used;
+      const uint64_t m2 = tc::pack_f32x2(sl2, sl2), b2 = tc::pack_f32x2(neg_mu, neg_mu);
+      // P = 2^(s * scale*log2(e) - max): packed FMA, MUFU ex2, bf16 pairs; the
+      // row sum adds the fp32 weights in four packed accumulators
       uint32_t pk[32];
-      float ls = 0.f;
+      uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const int hh = c >> 4, cc = (c & 15) * 2;
-        pk[c] = pack_bf16(exp2f(__uint_as_float(sr[hh][cc]) - mu),
-                          exp2f(__uint_as_float(sr[hh][cc + 1]) - mu));
-        ls += bf16_lo(pk[c]) + bf16_hi(pk[c]);
+        float y0, y1;
+        tc::fma_f32x2(x[2 * c], x[2 * c + 1], m2, b2, y0, y1);
+        y0 = ex2(y0);
+        y1 = ex2(y1);
+        pk[c] = pack_bf16(y0, y1);
+        tc::add_f32x2(acc[c & 3], y0, y1);
       }
+      const float ls = (tc::sum_f32x2(acc[0]) + tc::sum_f32x2(acc[1])) +
+                       (tc::sum_f32x2(acc[2]) + tc::sum_f32x2(acc[3]));
       l = l * alpha + ls;
       if (j > 0) {
-        if (!warp_wait(pv_done, (j - 1) & 1, abort, a.err)) { done = false; break; }
+        if (!warp_wait(b_pvdone, (j - 1) & 1, abort, a.err)) { done = false; break; }
         tc::fence_after_sync();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {   // rescale O in TMEM
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
-            tc::ld32(tmem + lane_off + kColO + c0, o);
+            tc::ld32(tO + c0, o);
             tc::wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tc::st32(tmem + lane_off + kColO + c0, o);
+            tc::st32(tO + c0, o);
           }
           tc::wait_st();
         }
       }
       if (j == ntiles - 1 && key0 + kTcKeys > pos_max + 1) {
         // Keys past pos_max have P = 0 in every row, but their V rows may be
-        // stale NaN or left over from an earlier tile: zero them.
+        // stale NaN or left over from an earlier tile: zero them before this
+        // warpgroup's P V product may be issued.  Both warpgroups do it (the
+        // MMAs of the two query tiles are issued in either order); the
+        // second writes zeros over zeros.
         if (!warp_wait(smem_u32(&sh->kv_full[j % kTcStages]), (j / kTcStages) & 1, abort,
                        a.err)) { done = false; break; }
         uint8_t* vt = sKV + (j % kTcStages) * Lt::kStageBytes + Lt::kKBytes;
@@ -362,20 +437,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
         fence_proxy_async();
       }
-      tc::st32(tmem + lane_off + kColP, pk);
+      tc::st32(tP, pk);
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(b_pfull);
     }
-    if (done && warp_wait(pv_done, (ntiles - 1) & 1, abort, a.err)) {
+    if (done && warp_wait(b_pvdone, (ntiles - 1) & 1, abort, a.err)) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        tc::ld32(tmem + lane_off + kColO + c0, o);
+        tc::ld32(tO + c0, o);
         tc::wait_ld();
         if (valid) {
           uint32_t w[16];
@@ -417,7 +492,8 @@ bool prefill_tc_supported(int head_size, int group) {
          kTcRows % group == 0;
 }
 
-int prefill_tc_tokens_per_cta(int group) { return kTcRows / group; }
+int prefill_tc_tokens_per_tile(int group) { return kTcRows / group; }
+int prefill_tc_tokens_per_cta(int group) { return kTcTiles * kTcRows / group; }
 
 cudaError_t launch_prefill_tc(const CUtensorMap& qmap, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const PrefillArgs& a, int head_size,

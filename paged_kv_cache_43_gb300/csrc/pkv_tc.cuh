@@ -113,5 +113,42 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
+// ---------------------------------------------------------------- softmax math
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two lanes of fp32 in one 64-bit register pair.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// (y0, y1) = (x0, x1) * m + b, lane-wise (packed f32x2 FMA).
+__device__ __forceinline__ void fma_f32x2(float x0, float x1, uint64_t m, uint64_t b, float& y0,
+                                          float& y1) {
+  asm("{\n\t.reg .b64 a, r;\n\tmov.b64 a, {%2, %3};\n\t"
+      "fma.rn.f32x2 r, a, %4, %5;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "l"(m), "l"(b));
+}
+
+// acc += (x0, x1), lane-wise (packed f32x2 add).
+__device__ __forceinline__ void add_f32x2(uint64_t& acc, float x0, float x1) {
+  asm("{\n\t.reg .b64 a;\n\tmov.b64 a, {%1, %2};\n\tadd.rn.f32x2 %0, %0, a;\n\t}"
+      : "+l"(acc)
+      : "f"(x0), "f"(x1));
+}
+
+__device__ __forceinline__ float sum_f32x2(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+
 }  // namespace tc
 }  // namespace pkv
