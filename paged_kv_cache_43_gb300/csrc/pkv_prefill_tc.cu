@@ -14,14 +14,18 @@
 //    holds 128/G tokens x G heads and is one TMA load per 64-column half
 //    (box 64 x G heads x 128/G tokens, 128-byte swizzle), which lands exactly
 //    in the K-major UMMA layout.
-//  * warp 0 streams 64-key K/V tiles (4 cache blocks, one TMA box per block
-//    and half) into a 4-stage ring shared by both query tiles; warp 1
+//  * warp 0 streams 128-key K and V tiles (8 cache blocks, one TMA box per
+//    block and half) into a 3-deep K ring and a 2-deep V ring (K is needed by
+//    the first product, V only by the second) shared by both query tiles; warp 1
 //    allocates all 512 TMEM columns and one of its threads issues every MMA:
-//        S_t  = Q_t K^T   (M=128, N=64, K=16 x D/16, operands from smem)
-//        O_t += P_t V     (M=128, N=D,  K=16 x 4, P_t from TMEM, V MN-major)
-//    for the two tiles t in turn, so the tensor core works on one tile while
-//    the softmax of the other runs, and S_t of the next K/V tile is computed
-//    as soon as the softmax has read the current one.
+//        S_t  = Q_t K^T   (M=128, N=128, K=16 x D/16, operands from smem)
+//        O_t += P_t V     (M=128, N=D,   K=16 x 8, P_t from TMEM, V MN-major)
+//    An M=128 tcgen05 MMA takes the same time for any N <= 256, so the tiles
+//    are as wide as TMEM allows: S_t (128 columns) and O_t (D columns) per
+//    query tile fill the 512 columns, and P_t (bf16) is written over the
+//    first half of S_t's columns.  S_t of the next K/V tile is issued once
+//    P_t V has completed; meanwhile the tensor core runs the other query
+//    tile's products, so it is never waiting on one softmax.
 //  * warps 2-5 and 6-9 (one warpgroup per query tile) own one TMEM lane
 //    (= one row) per thread: they load a row of S, apply the causal mask, keep
 //    a lazily updated running max (O is rescaled in TMEM only when the max
@@ -40,13 +44,15 @@ namespace {
 
 constexpr int kTcRows = 128;      // UMMA M (rows of one query tile)
 constexpr int kTcTiles = 2;       // query tiles per CTA
-constexpr int kTcKeys = 64;       // keys per K/V tile
+constexpr int kTcKeys = 128;      // keys per K/V tile
 constexpr int kTcThreads = 320;   // load, MMA, 2 x 4 softmax warps
-constexpr int kTcStages = 4;
+constexpr int kKStages = 3;       // K ring depth
+constexpr int kVStages = 2;       // V ring depth
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S of tile t at 64t, P of tile t at 128 + 32t, O of tile t at 256 + 128t.
-__host__ __device__ constexpr uint32_t col_s(int t) { return 64u * t; }
-__host__ __device__ constexpr uint32_t col_p(int t) { return 128u + 32u * t; }
+// TMEM columns: S of tile t at 128t (P of tile t over its first 64 columns),
+// O of tile t at 256 + 128t.
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }
+__host__ __device__ constexpr uint32_t col_p(int t) { return 128u * t; }
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
 constexpr float kLazyRescale = 8.0f;  // log2 units: rescale O only past 2^8 growth
 
@@ -55,15 +61,14 @@ struct TcLayout {
   static constexpr int kHalves = D / 64;
   static constexpr int kQHalf = kTcRows * 128;       // 16 KB: 128 rows x 128 B
   static constexpr int kQTile = kHalves * kQHalf;
-  static constexpr int kKvHalf = kTcKeys * 128;      // 8 KB: 64 keys x 128 B
-  static constexpr int kKBytes = kHalves * kKvHalf;
-  static constexpr int kStageBytes = 2 * kKBytes;    // K then V
+  static constexpr int kKvHalf = kTcKeys * 128;      // 16 KB: 128 keys x 128 B
+  static constexpr int kTileBytes = kHalves * kKvHalf;  // one K (or V) tile
 };
 
 struct TcShared {
   uint64_t q_full, drain;
-  uint64_t s_full[kTcTiles], s_free[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
-  uint64_t kv_full[kTcStages], kv_empty[kTcStages];
+  uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -72,7 +77,8 @@ template <int D>
 constexpr int tc_smem_bytes() {
   // Whole-SM footprint: one CTA per SM (it owns all 512 TMEM columns).
   constexpr int need = 1024 + kTcTiles * TcLayout<D>::kQTile +
-                       kTcStages * TcLayout<D>::kStageBytes + static_cast<int>(sizeof(TcShared));
+                       (kKStages + kVStages) * TcLayout<D>::kTileBytes +
+                       static_cast<int>(sizeof(TcShared));
   return need > 120 * 1024 ? need : 120 * 1024;
 }
 
@@ -122,8 +128,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                                   // [tile][half][128 rows x 128 B]
-  uint8_t* sKV = smem + kTcTiles * Lt::kQTile;          // [stage][K halves | V halves]
-  TcShared* sh = reinterpret_cast<TcShared*>(sKV + kTcStages * Lt::kStageBytes);
+  uint8_t* sK = smem + kTcTiles * Lt::kQTile;           // [K stage][half][128 keys x 128 B]
+  uint8_t* sV = sK + kKStages * Lt::kTileBytes;         // [V stage][half][128 keys x 128 B]
+  TcShared* sh = reinterpret_cast<TcShared*>(sV + kVStages * Lt::kTileBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -173,13 +180,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(drain, 1);
     for (int t = 0; t < kTcTiles; ++t) {
       mbar_init(smem_u32(&sh->s_full[t]), 1);
-      mbar_init(smem_u32(&sh->s_free[t]), 4);
       mbar_init(smem_u32(&sh->p_full[t]), 4);
       mbar_init(smem_u32(&sh->pv_done[t]), 1);
     }
-    for (int i = 0; i < kTcStages; ++i) {
-      mbar_init(smem_u32(&sh->kv_full[i]), 1);
-      mbar_init(smem_u32(&sh->kv_empty[i]), 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(smem_u32(&sh->k_full[i]), 1);
+      mbar_init(smem_u32(&sh->k_empty[i]), 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(smem_u32(&sh->v_full[i]), 1);
+      mbar_init(smem_u32(&sh->v_empty[i]), 1);
     }
     sh->abort = 0;
     fence_barrier_init();
@@ -203,47 +213,64 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_load_3d(smem_u32(sQ + t * Lt::kQTile + h * Lt::kQHalf), &qmap, q_full, h * 64,
                       kvh * G, q0 + tok0 + t * tile_toks, keep);
     }
-    int my_bid = -1;
-    for (int it = 0; it < ntiles; ++it) {
-      const int st = it % kTcStages;
-      if (it >= kTcStages &&
-          !warp_wait(smem_u32(&sh->kv_empty[st]), ((it / kTcStages) - 1) & 1, abort, a.err))
-        break;
-      if ((it & 7) == 0) {  // block ids of the next 8 tiles, one per lane
-        const int b = it * 4 + lane;
-        my_bid = b < nblk ? __ldg(bt + b) : -1;
-      }
-      bool ok[4];
-      int bid[4];
+    // Lanes 0..7 hold the block ids of one tile (ids of tile it + 1 are loaded
+    // while tile it is issued).  K of tile it goes out before V of tile it - 1.
+    constexpr int kBlocks = kTcKeys / kBlock;      // cache blocks per tile
+    auto load_ids = [&](int it) {
+      const int b = it * kBlocks + lane;
+      return (lane < kBlocks && it < ntiles && b < nblk) ? __ldg(bt + b) : -1;
+    };
+    // Issues the K (is_v = false) or V tile `it` into `dst`, completing on `full`.
+    auto issue_tile = [&](int it, int ids, bool is_v, uint32_t dst, uint32_t full) {
+      bool ok[kBlocks];
+      int bid[kBlocks];
       uint32_t bytes = 0;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        bid[b] = __shfl_sync(0xffffffffu, my_bid, (it & 7) * 4 + b);
-        const bool in_range = it * 4 + b < nblk;
+      for (int b = 0; b < kBlocks; ++b) {
+        bid[b] = __shfl_sync(0xffffffffu, ids, b);
+        const bool in_range = it * kBlocks + b < nblk;
         ok[b] = in_range && bid[b] >= 0 && bid[b] < a.num_blocks;
-        if (in_range && !ok[b] && lane == 0) raise_error(a.err, PKV_ERR_BLOCK_ID);
-        bytes += ok[b] ? 2u * Lt::kHalves * 2048u : 0u;
+        if (!is_v && in_range && !ok[b] && lane == 0) raise_error(a.err, PKV_ERR_BLOCK_ID);
+        bytes += ok[b] ? Lt::kHalves * 2048u : 0u;
       }
       if (lane == 0) {
-        const uint32_t full = smem_u32(&sh->kv_full[st]);
-        const uint32_t dst = smem_u32(sKV + st * Lt::kStageBytes);
         if (bytes == 0) {
           mbar_arrive(full);
         } else {
           mbar_arrive_expect_tx(full, bytes);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+          for (int b = 0; b < kBlocks; ++b) {
             if (!ok[b]) continue;
 #pragma unroll
-            for (int h = 0; h < Lt::kHalves; ++h) {
-              tma_load_3d(dst + h * Lt::kKvHalf + b * 2048, &kmap, full, h * 64, kvh,
-                          bid[b] * kBlock, keep);
-              tma_load_3d(dst + Lt::kKBytes + h * Lt::kKvHalf + b * 2048, &vmap, full, h * 64,
+            for (int h = 0; h < Lt::kHalves; ++h)
+              tma_load_3d(dst + h * Lt::kKvHalf + b * 2048, is_v ? &vmap : &kmap, full, h * 64,
                           kvh, bid[b] * kBlock, keep);
-            }
           }
         }
       }
+    };
+    int ids_cur = load_ids(0), ids_prev = -1;
+    for (int it = 0; it <= ntiles; ++it) {
+      const int ids_next = load_ids(it + 1);
+      if (it < ntiles) {
+        const int st = it % kKStages;
+        if (it >= kKStages &&
+            !warp_wait(smem_u32(&sh->k_empty[st]), ((it / kKStages) - 1) & 1, abort, a.err))
+          break;
+        issue_tile(it, ids_cur, false, smem_u32(sK + st * Lt::kTileBytes),
+                   smem_u32(&sh->k_full[st]));
+      }
+      if (it >= 1) {
+        const int iv = it - 1;
+        const int st = iv % kVStages;
+        if (iv >= kVStages &&
+            !warp_wait(smem_u32(&sh->v_empty[st]), ((iv / kVStages) - 1) & 1, abort, a.err))
+          break;
+        issue_tile(iv, ids_prev, true, smem_u32(sV + st * Lt::kTileBytes),
+                   smem_u32(&sh->v_full[st]));
+      }
+      ids_prev = ids_cur;
+      ids_cur = ids_next;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -252,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
       auto issue_s = [&](int t, int j) {
         const uint32_t q_addr = smem_u32(sQ + t * Lt::kQTile);
-        const uint32_t k_addr = smem_u32(sKV + (j % kTcStages) * Lt::kStageBytes);
+        const uint32_t k_addr = smem_u32(sK + (j % kKStages) * Lt::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;  // 16 bf16 = 32 B along the swizzled row
@@ -265,8 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::commit(smem_u32(&sh->s_full[t]));
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t v_addr =
-            smem_u32(sKV + (j % kTcStages) * Lt::kStageBytes + Lt::kKBytes);
+        const uint32_t v_addr = smem_u32(sV + (j % kVStages) * Lt::kTileBytes);
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks) {
           const uint64_t dv = tc::smem_desc_sw128(v_addr + ks * 2048, Lt::kKvHalf, 1024);
@@ -276,39 +302,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::commit(smem_u32(&sh->pv_done[t]));
       };
       // Event loop: issue whichever MMA is ready, never blocking on one
-      // tile while the other could use the tensor core.  Phases cannot run
-      // more than one ahead of what this thread has seen, so parity probes
-      // are unambiguous.
+      // query tile while the other could use the tensor core.  No barrier
+      // phase can run more than one ahead of what this thread has seen, so
+      // parity probes are unambiguous.
       int s_next[kTcTiles] = {0, 0};   // next tile index whose S is issued
       int pv_next[kTcTiles] = {0, 0};  // next tile index whose P V is issued
-      int released = 0;                // K/V stages handed back to the producer
+      int k_released = 0, v_released = 0;  // ring stages handed back to the producer
       bool ok = wait_or_abort(q_full, 0, abort, a.err);
       uint64_t idle_since = 0;
       while (ok) {
         bool progress = false;
         for (int t = 0; t < ntq; ++t) {
-          const int js = s_next[t];
-          if (js < ntiles &&
-              mbar_test(smem_u32(&sh->kv_full[js % kTcStages]), (js / kTcStages) & 1) &&
-              (js == 0 || mbar_test(smem_u32(&sh->s_free[t]), (js - 1) & 1))) {
-            tc::fence_after_sync();
-            issue_s(t, js);
-            s_next[t] = js + 1;
-            progress = true;
-          }
           const int jp = pv_next[t];
-          if (jp < s_next[t] && mbar_test(smem_u32(&sh->p_full[t]), jp & 1)) {
+          if (jp < s_next[t] && mbar_test(smem_u32(&sh->p_full[t]), jp & 1) &&
+              mbar_test(smem_u32(&sh->v_full[jp % kVStages]), (jp / kVStages) & 1)) {
             tc::fence_after_sync();
             issue_pv(t, jp);
             pv_next[t] = jp + 1;
             progress = true;
           }
+          const int js = s_next[t];
+          // S_t(js) overwrites the columns P_t(js - 1) lives in.  MMAs issued
+          // by one thread execute in issue order, so issuing it right after
+          // P_t(js - 1) V is enough; doing so at once makes the tensor-core
+          // order P0 V, S0, P1 V, S1 and offsets the two softmaxes by half a
+          // period, so one runs while the other tile's products do.
+          if (js < ntiles && pv_next[t] == js &&
+              mbar_test(smem_u32(&sh->k_full[js % kKStages]), (js / kKStages) & 1)) {
+            tc::fence_after_sync();
+            issue_s(t, js);
+            s_next[t] = js + 1;
+            progress = true;
+          }
         }
-        int done_pv = pv_next[0];
-        if (ntq > 1) done_pv = min(done_pv, pv_next[1]);
-        while (released < done_pv) {  // every P V of that stage is issued
-          tc::commit(smem_u32(&sh->kv_empty[released % kTcStages]));
-          ++released;
+        int done_s = s_next[0], done_pv = pv_next[0];
+        if (ntq > 1) {
+          done_s = min(done_s, s_next[1]);
+          done_pv = min(done_pv, pv_next[1]);
+        }
+        while (k_released < done_s) {  // both S products of that K tile issued
+          tc::commit(smem_u32(&sh->k_empty[k_released % kKStages]));
+          ++k_released;
+        }
+        while (v_released < done_pv) {  // both P V products of that V tile issued
+          tc::commit(smem_u32(&sh->v_empty[v_released % kVStages]));
+          ++v_released;
         }
         if (done_pv == ntiles) break;
         if (progress) {
@@ -342,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool valid = tok <= tok_last;
     const int pos = L - qn + (valid ? tok : tok_last);
     const int ts = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the warpgroup
-    const uint32_t b_sfull = smem_u32(&sh->s_full[t]), b_sfree = smem_u32(&sh->s_free[t]);
+    const uint32_t b_sfull = smem_u32(&sh->s_full[t]);
     const uint32_t b_pfull = smem_u32(&sh->p_full[t]), b_pvdone = smem_u32(&sh->pv_done[t]);
     const uint32_t tS = tmem + lane_off + col_s(t), tP = tmem + lane_off + col_p(t);
     const uint32_t tO = tmem + lane_off + col_o(t);
@@ -350,21 +388,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool done = t < ntq;
     for (int j = 0; done && j < ntiles; ++j) {
+      // S_t(j) complete (its commit also covers P_t(j - 1) V, so O_t is stable)
       if (!warp_wait(b_sfull, j & 1, abort, a.err)) { done = false; break; }
       tc::fence_after_sync();
-      uint32_t sr[2][32];
-      tc::ld32(tS, sr[0]);
-      tc::ld32(tS + 32, sr[1]);
+      float x[kTcKeys];
+#pragma unroll
+      for (int c0 = 0; c0 < kTcKeys; c0 += 32) {
+        uint32_t r[32];
+        tc::ld32(tS + c0, r);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[c0 + c] = __uint_as_float(r[c]);
+      }
       tc::wait_ld();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_sfree);
       // causal mask on raw scores (also hides keys >= L); scale > 0, so the
       // row max of the raw scores gives the max of the scaled ones
       const int key0 = j * kTcKeys;
-      float x[kTcKeys];
-#pragma unroll
-      for (int c = 0; c < kTcKeys; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
       if (key0 + kTcKeys - 1 > pos) {
 #pragma unroll
         for (int c = 0; c < kTcKeys; ++c) x[c] = (key0 + c > pos) ? -INFINITY : x[c];
@@ -372,12 +410,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // row max: four independent chains of three-input maxima
       float m4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-      for (int c = 4; c < kTcKeys; c += 8) {
+      for (int c = 4; c < kTcKeys - 4; c += 8) {
         m4[0] = tc::max3(m4[0], x[c], x[c + 1]);
         m4[1] = tc::max3(m4[1], x[c + 2], x[c + 3]);
         m4[2] = tc::max3(m4[2], x[c + 4], x[c + 5]);
         m4[3] = tc::max3(m4[3], x[c + 6], x[c + 7]);
       }
+      m4[0] = tc::max3(m4[0], x[kTcKeys - 4], x[kTcKeys - 3]);
+      m4[1] = tc::max3(m4[1], x[kTcKeys - 2], x[kTcKeys - 1]);
       const float mt = tc::max3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
       float alpha = 1.f;
       if (mt > m_used + kLazyRescale) {
@@ -386,47 +426,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const float neg_mu = (m_used == -INFINITY) ? 0.f : -m_used;
       const uint64_t m2 = tc::pack_f32x2(sl2, sl2), b2 = tc::pack_f32x2(neg_mu, neg_mu);
-      // P = 2^(s * scale*log2(e) - max): packed FMA, MUFU ex2, bf16 pairs; the
-      // row sum adds the fp32 weights in four packed accumulators
-      uint32_t pk[32];
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {   // rescale O in TMEM
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tc::ld32(tO + c0, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tc::st32(tO + c0, o);
+        }
+      }
+      // P = 2^(s * scale*log2(e) - max): packed FMA, MUFU ex2, bf16 pairs
+      // written over S's first 64 columns; the row sum adds the fp32 weights
       uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        float y0, y1;
-        tc::fma_f32x2(x[2 * c], x[2 * c + 1], m2, b2, y0, y1);
-        y0 = ex2(y0);
-        y1 = ex2(y1);
-        pk[c] = pack_bf16(y0, y1);
-        tc::add_f32x2(acc[c & 3], y0, y1);
+      for (int c0 = 0; c0 < kTcKeys / 2; c0 += 32) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int k = 2 * (c0 + c);
+          float y0, y1;
+          tc::fma_f32x2(x[k], x[k + 1], m2, b2, y0, y1);
+          y0 = ex2(y0);
+          y1 = ex2(y1);
+          pk[c] = pack_bf16(y0, y1);
+          tc::add_f32x2(acc[c & 3], y0, y1);
+        }
+        tc::st32(tP + c0, pk);
       }
       const float ls = (tc::sum_f32x2(acc[0]) + tc::sum_f32x2(acc[1])) +
                        (tc::sum_f32x2(acc[2]) + tc::sum_f32x2(acc[3]));
       l = l * alpha + ls;
-      if (j > 0) {
-        if (!warp_wait(b_pvdone, (j - 1) & 1, abort, a.err)) { done = false; break; }
-        tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {   // rescale O in TMEM
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tc::ld32(tO + c0, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tc::st32(tO + c0, o);
-          }
-          tc::wait_st();
-        }
-      }
       if (j == ntiles - 1 && key0 + kTcKeys > pos_max + 1) {
         // Keys past pos_max have P = 0 in every row, but their V rows may be
         // stale NaN or left over from an earlier tile: zero them before this
         // warpgroup's P V product may be issued.  Both warpgroups do it (the
         // MMAs of the two query tiles are issued in either order); the
         // second writes zeros over zeros.
-        if (!warp_wait(smem_u32(&sh->kv_full[j % kTcStages]), (j / kTcStages) & 1, abort,
+        if (!warp_wait(smem_u32(&sh->v_full[j % kVStages]), (j / kVStages) & 1, abort,
                        a.err)) { done = false; break; }
-        uint8_t* vt = sKV + (j % kTcStages) * Lt::kStageBytes + Lt::kKBytes;
+        uint8_t* vt = sV + (j % kVStages) * Lt::kTileBytes;
         const int first = pos_max + 1 - key0;
         const int per_row = Lt::kHalves * 8;
         for (int e = ts; e < (kTcKeys - first) * per_row; e += 128) {
@@ -437,7 +477,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         fence_proxy_async();
       }
-      tc::st32(tP, pk);
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
