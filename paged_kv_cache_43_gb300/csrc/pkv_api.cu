@@ -147,16 +147,19 @@ int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan
   if (m->kv_split_tokens > 0) {
     split_blocks = m->kv_split_tokens / kBlock;
   } else {
-    // 512-key chunks (256 KB of K+V per head at D=128) balance the uneven
-    // context lengths of a decode batch; shorter chunks only when the batch
-    // has too few (sequence, head) units to fill the GPU twice over.
+    // Chunk of keys per CTA, measured on GB300 decode batches: 1024 keys
+    // (512 KB of K+V per kv head at D=128) by default; 2048 for long contexts
+    // (>= 16K keys), which halves the split partials and the CTAs that find
+    // nothing to do, as long as that still leaves four waves of CTAs; shorter
+    // chunks only when the batch has too few (sequence, head) units to fill
+    // the GPU twice over.
     const int g_sub = (m->num_q_heads / c->num_kv_heads + 7) / 8;
     const int64_t units = static_cast<int64_t>(nd) * c->num_kv_heads * g_sub;
-    const int64_t want = 2LL * num_sms * 2;  // two waves of two CTAs per SM
-    split_blocks = 32;
-    while (split_blocks > 4 &&
-           units * ((max_blocks + split_blocks - 1) / split_blocks) < want)
-      split_blocks /= 2;
+    const int64_t slots = 2LL * num_sms;  // two CTAs per SM
+    auto ctas = [&](int sb) { return units * ((max_blocks + sb - 1) / sb); };
+    split_blocks = 64;
+    if (m->max_context_len >= 16384 && ctas(128) >= 4 * slots) split_blocks = 128;
+    while (split_blocks > 4 && ctas(split_blocks) < 2 * slots) split_blocks /= 2;
   }
   p->split_blocks = split_blocks;
   p->max_splits = max_blocks > 0 ? (max_blocks + split_blocks - 1) / split_blocks : 1;

@@ -341,9 +341,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 }
 
 // ---------------------------------------------------------------- combine
-// One warp per (sequence, q head): out = sum_i 2^(lse_i - M) O_i / sum_i 2^(lse_i - M).
+// One warp per (sequence, q head) whose context was split:
+// out = sum_i 2^(lse_i - M) O_i / sum_i 2^(lse_i - M).  The step is
+// latency-bound, so the split loop is unrolled eight deep: a lane issues the
+// loads of eight partial rows (a float4 or float2 of the head each) and their
+// log-sum-exps before it needs any of them.
+constexpr int kCombineUnroll = 8;
+
 template <int D>
 __global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs a) {
+  constexpr int PER = D / 32;  // elements per lane
+  static_assert(PER == 2 || PER % 4 == 0, "head_size 64 or a multiple of 128");
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= a.num_seqs * a.num_q_heads) return;
@@ -358,30 +366,44 @@ __global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs 
   const int nsplit = ((L + kBlock - 1) / kBlock + a.split_blocks - 1) / a.split_blocks;
   if (nsplit <= 1) return;  // the decode kernel wrote this row directly
   const int64_t row = (static_cast<int64_t>(s) * a.num_q_heads + hq) * a.max_splits;
+  const float* lse = a.ws_lse + row;
   float M = -INFINITY;
-  for (int i = lane; i < nsplit; i += 32) M = fmaxf(M, a.ws_lse[row + i]);
+  for (int i = lane; i < nsplit; i += 32) M = fmaxf(M, lse[i]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  constexpr int PER = D / 32;  // elements per lane
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float den = 0.f;
   if (M != -INFINITY) {
-    for (int i = 0; i < nsplit; ++i) {
-      const float lse = a.ws_lse[row + i];
-      const float w = (lse == -INFINITY) ? 0.f : exp2f(lse - M);
-      den += w;
-      const float* oi = a.ws_o + (row + i) * D + lane * PER;
-      if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(oi);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2] += w * v.z;
-        acc[3] += w * v.w;
-      } else {
+    const float* o = a.ws_o + row * D + lane * PER;
+    for (int i0 = 0; i0 < nsplit; i0 += kCombineUnroll) {
+      float v[kCombineUnroll][PER];
+      float lv[kCombineUnroll];
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] += w * oi[e];
+      for (int u = 0; u < kCombineUnroll; ++u) {
+        const int i = i0 + u;
+        lv[u] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) v[u][e] = 0.f;
+        if (i < nsplit) {
+          lv[u] = lse[i];
+          const float* src = o + static_cast<int64_t>(i) * D;
+          if constexpr (PER == 2) {
+            *reinterpret_cast<float2*>(v[u]) = *reinterpret_cast<const float2*>(src);
+          } else {
+#pragma unroll
+            for (int e = 0; e < PER; e += 4)
+              *reinterpret_cast<float4*>(v[u] + e) = *reinterpret_cast<const float4*>(src + e);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kCombineUnroll; ++u) {
+        const float w = (lv[u] == -INFINITY) ? 0.f : exp2f(lv[u] - M);
+        den += w;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] += w * v[u][e];
       }
     }
   }

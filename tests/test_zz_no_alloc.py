@@ -63,7 +63,8 @@ def test_static_scratch_matches_workspace_call_twice(n, split):
 
 def test_static_scratch_rejects_batches_beyond_its_size():
     g = W.workload(2, small=True).to("cuda")
-    big = dict(max_query_len=1, max_context_len=1 << 20, num_decode_seqs=-1,
+    # valid (1024 splits of 64 keys) but ~101 MB of split-K workspace
+    big = dict(max_query_len=1, max_context_len=1 << 16, num_decode_seqs=-1,
                kv_split_tokens=64)
     meta = pkv.attn_meta(g.q, g.block_tables, g.context_lens, **big)
     assert pkv.workspace_size(g.k_cache, meta) > pkv.STATIC_SCRATCH_BYTES
