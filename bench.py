@@ -48,6 +48,26 @@ def _env_int(name, default):
         return default
 
 
+def rank_seed(workload: int, rank: int) -> int:
+    """Each rank draws its own batch of the same shape (independent replicas)."""
+    from paged_kv_cache_43_gb300 import workloads as W
+    return W.SEED_BASE + workload + 1000 * rank
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's time: the whole job is done when it is."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank moves its own bytes in the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -233,7 +253,7 @@ def run_pkv(args, rank, world, device):
 
     build.build()
     pkv.load()
-    wl = W.workload(args.workload, device=device, seed=W.SEED_BASE + args.workload + 1000 * rank,
+    wl = W.workload(args.workload, device=device, seed=rank_seed(args.workload, rank),
                     num_seqs=args.num_seqs)
     if args.profile:
         return profile_only(args, wl)
@@ -300,10 +320,7 @@ def run_pkv(args, rank, world, device):
     # parity spot check on the timed output: a few rows against the oracle
     parity = spot_check(wl, out, spot)
 
-    t = torch.tensor([total_ms], device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / args.steps
 
     # ---- end to end: host buffers in, host result out, same stream
@@ -312,7 +329,7 @@ def run_pkv(args, rank, world, device):
     if rank != 0:
         return None
     peak, peak_kind = hbm_peak()
-    value = world * step_b / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput(step_b, world, ms_per_step)
     achieved = attn_b / (attn_ms * 1e-3) / 1e9
     traffic = recorded_traffic(wl.name)
     line = {

@@ -295,3 +295,41 @@ def test_full_size_step_sampled_against_oracle(n):
                     assert st == 0
                     errs.append(np.abs(got[q0 + j, h] - acc / l).max())
         assert max(errs) <= 2e-2, max(errs)
+
+
+# ------------------------------------------------------------ CUDA graphs
+
+def test_step_captured_in_a_cuda_graph_replays_correctly():
+    """The calls only enqueue work (no allocation, no synchronisation), so a
+    whole step -- write, split-K attention, combine -- can be captured once and
+    replayed; replays pick up new inputs written into the same buffers."""
+    wl = W.workload(5, small=True)
+    exp, _, _, _ = oracle_step(wl)
+    g = wl.to("cuda")
+    meta = pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=1,
+                         max_context_len=g.max_context_len, kv_split_tokens=128)
+    ws = torch.empty(pkv.workspace_size(g.k_cache, meta), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    out = torch.empty_like(g.q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):   # first call on the device: set-up outside the capture
+        pkv.run_step(g, out, workspace=ws, kv_split_tokens=128)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        pkv.run_step(g, out, workspace=ws, kv_split_tokens=128)
+    out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert max_err(out, exp) <= 2e-2
+    # new queries in the same buffer, replay again
+    q2 = torch.randn(wl.q.shape, generator=torch.Generator().manual_seed(99)).to(wl.q.dtype)
+    wl2 = W.Workload(**{k: getattr(wl, k) for k in wl.__dataclass_fields__})
+    wl2.q = q2
+    exp2, _, _, _ = oracle_step(wl2)
+    g.q.copy_(q2)
+    out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert max_err(out, exp2) <= 2e-2
+    assert pkv.get_error() == 0
