@@ -54,6 +54,7 @@ class OrcProblem(ctypes.Structure):
         ("num_blocks", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
         ("scale", ctypes.c_double),
+        ("window", ctypes.c_int32),
     ]
 
 
@@ -138,7 +139,7 @@ class Problem:
     """Keeps the numpy buffers of one attention problem alive for ctypes."""
 
     def __init__(self, q, k_cache, v_cache, block_tables, context_lens,
-                 query_start_loc, scale):
+                 query_start_loc, scale, window: int = 0):
         self.q = _raw(q)
         self.k_cache = _raw(k_cache)
         self.v_cache = _raw(v_cache)
@@ -157,19 +158,20 @@ class Problem:
             _ptr(self.q), _ptr(self.k_cache), _ptr(self.v_cache),
             _ptr(self.block_tables), _ptr(self.context_lens), _ptr(self.query_start_loc),
             self.block_tables.shape[1] if self.block_tables.ndim == 2 else 0,
-            s, hq, hkv, d, bs, nb, code, float(scale))
+            s, hq, hkv, d, bs, nb, code, float(scale), int(window))
 
 
 def attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
-              scale, nthreads: int = 0):
+              scale, nthreads: int = 0, window: int = 0):
     """Exact paged attention in fp64 (ch. 6 "Structure des métadonnées",
-    "Flux des paramètres du chemin non-cascadé", "Branche de masque").
+    "Flux des paramètres du chemin non-cascadé", "Branche de masque"); with
+    ``window`` W > 0 a query at position pos sees keys pos - W < p <= pos.
 
     Returns ``(out, seq_status)``: ``out`` is float64 [T, Hq, D]; rows of a
     sequence with status 1 (metadata error) are zero, status 2 (block id out of
     range) NaN."""
     lib = _load()
-    P = Problem(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale)
+    P = Problem(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, window)
     out = np.zeros((P.num_tokens, P.shape["Hq"], P.shape["D"]), dtype=np.float64)
     status = np.zeros(P.shape["S"], dtype=np.int32)
     lib.orc_attention(ctypes.byref(P.c), _ptr(out), _ptr(status), int(nthreads))

@@ -33,8 +33,10 @@ def dense_kv(k_cache, v_cache, block_row, L):
     return flat_k[slots], flat_v[slots]
 
 
-def attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale):
-    """float64 [T, Hq, D]; valid inputs only."""
+def attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
+              window=0):
+    """float64 [T, Hq, D]; valid inputs only.  ``window`` W > 0 restricts the
+    query at position pos to keys pos - W < p <= pos."""
     qf = widen(q)
     T, hq, d = qf.shape
     hkv = k_cache.shape[2]
@@ -48,6 +50,8 @@ def attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, 
         K, V = dense_kv(k_cache, v_cache, block_tables[s], L)
         pos = L - n + np.arange(n)                       # absolute positions
         visible = np.arange(L)[None, :] <= pos[:, None]  # [n, L]
+        if window > 0:
+            visible &= np.arange(L)[None, :] > (pos[:, None] - window)
         for h in range(hq):
             kv = h // g
             x = scale * (qf[q0:q1, h, :] @ K[:, kv, :].T)  # [n, L]

@@ -34,6 +34,12 @@
  *    GQA: query head hq reads kv head hq / (num_q_heads / num_kv_heads)
  *    (contiguous groups; the pages do not state the mapping).
  *
+ *  - Sliding window ([book] ch. 2 "FullAttentionSpec", ch. 4 §4.1 null block,
+ *    ch. 6 "Flux des paramètres": causal window (w, 0)): with window W > 0 the
+ *    query at position pos sees only keys pos - W < p <= pos (W keys including
+ *    itself); block-table entries wholly before that range are never read (they
+ *    may hold the null block).  W = 0 means no window.
+ *
  *  - Partial state and merge (the split buffer of [book] ch. 6 "build() étape
  *    par étape", fourth step, and merge_attn_states in the ch. 6 sequence
  *    diagram): a key range yields (m, l, acc) = (max x, sum e^(x-m),
@@ -66,6 +72,7 @@ typedef struct {
   int32_t num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks;
   int32_t dtype;              /* ORC_F32 or ORC_BF16 */
   double scale;
+  int32_t window;             /* sliding window W (keys per query), 0 = none */
 } orc_problem;
 
 /* One stored element, widened exactly to double.  bf16 is the top half of an
@@ -136,6 +143,7 @@ int orc_row_state(const orc_problem *P, int32_t s, int32_t hq, int32_t j,
   const int64_t pos = (int64_t)L - q_len + j;      /* absolute query position */
   int64_t hi = p_hi < pos + 1 ? p_hi : pos + 1;    /* causal: keys p <= pos */
   int64_t lo = p_lo < 0 ? 0 : p_lo;
+  if (P->window > 0 && lo < pos - P->window + 1) lo = pos - P->window + 1;  /* window */
   if (hi <= lo) return 0;
 
   const int64_t t = P->query_start_loc[s] + j;

@@ -333,3 +333,57 @@ def test_metadata_errors_zero_rows():
     out, st = oracle.attention(q, kc, vc, bt, cl, qsl, sc)
     assert st.tolist() == [1, 2]
     assert (out[0] == 0).all() and np.isnan(out[1]).all()
+
+
+# ------------------------------------------------------------ sliding window
+
+def test_window_wider_than_context_is_full_attention():
+    wl = W.make_workload([1, 7, 1], [40, 55, 90], num_q_heads=4, num_kv_heads=2, head_size=64,
+                         dtype=torch.bfloat16, seed=21)
+    args = _written(wl)
+    full, _ = oracle.attention(*args)
+    wide, st = oracle.attention(*args, window=90)
+    assert not st.any()
+    np.testing.assert_array_equal(full, wide)
+
+
+def test_window_of_one_gives_the_query_own_value():
+    wl = W.make_workload([1, 5], [37, 50], num_q_heads=2, num_kv_heads=1, head_size=64,
+                         dtype=torch.float32, seed=22)
+    q, kc, vc, bt, cl, qsl, sc = _written(wl)
+    out, st = oracle.attention(q, kc, vc, bt, cl, qsl, sc, window=1)
+    assert not st.any()
+    vf = vc.reshape(-1, 1, 64).astype(np.float64)
+    for s, (n, L) in enumerate([(1, 37), (5, 50)]):
+        for j in range(n):
+            pos = L - n + j
+            slot = int(bt[s, pos // 16]) * 16 + pos % 16
+            t = int(qsl[s]) + j
+            for h in range(2):
+                np.testing.assert_array_equal(out[t, h], vf[slot, 0])
+
+
+@pytest.mark.parametrize("window", [2, 16, 17, 40])
+def test_window_matches_brute_force(window):
+    wl = W.make_workload([1, 20, 1, 33], [70, 64, 17, 100], num_q_heads=8, num_kv_heads=2,
+                         head_size=64, dtype=torch.bfloat16, seed=23)
+    args = _written(wl)
+    out, st = oracle.attention(*args, window=window)
+    assert not st.any()
+    np.testing.assert_allclose(out, brute.attention(*args, window=window), atol=1e-12,
+                               rtol=1e-10)
+
+
+def test_window_never_reads_blocks_before_the_window():
+    """Entries for blocks wholly before every query's window may hold the null
+    block (here: an invalid id); results must not change."""
+    wl = W.make_workload([1, 4], [100, 90], num_q_heads=2, num_kv_heads=2, head_size=64,
+                         dtype=torch.bfloat16, seed=24)
+    q, kc, vc, bt, cl, qsl, sc = _written(wl)
+    out, _ = oracle.attention(q, kc, vc, bt, cl, qsl, sc, window=20)
+    bt2 = bt.copy()
+    bt2[0, : (100 - 20) // 16] = -1              # keys < 80 are outside every window
+    bt2[1, : (90 - 4 - 20 + 1) // 16] = -1       # first query at 86 sees keys > 66
+    out2, st = oracle.attention(q, kc, vc, bt2, cl, qsl, sc, window=20)
+    assert not st.any()
+    np.testing.assert_array_equal(out, out2)
