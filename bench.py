@@ -100,14 +100,16 @@ def recorded_traffic(workload_name: str):
     return rec.get("per_workload", {}).get(workload_name)
 
 
-def algorithmic_bytes(wl):
+def algorithmic_bytes(wl, window=0):
     """Bytes the step must move at minimum.
-    attention: each visible K and V row once, q read, out written, the block
-    table entries and per-sequence metadata read;
-    write: new K/V rows read and written, slots read."""
+    attention: each K and V row some query of its sequence can see, once; q
+    read, out written, the block-table entries of those rows and per-sequence
+    metadata read; write: new K/V rows read and written, slots read."""
     e = wl.q.element_size()
     hkv, d, hq = wl.num_kv_heads, wl.head_size, wl.num_q_heads
     ctx = wl.ctx_lens.astype(np.int64)
+    if window > 0:   # keys [L - q_s - W + 1, L) are visible to some row
+        ctx = ctx - np.maximum(0, ctx - wl.q_lens.astype(np.int64) - window + 1)
     kv = int(ctx.sum()) * hkv * d * e * 2
     qo = 2 * wl.num_tokens * hq * d * e
     meta = int(np.ceil(ctx / 16).sum()) * 4 + wl.num_seqs * 4 + (wl.num_seqs + 1) * 4
@@ -205,28 +207,32 @@ def oracle_sample(wl_gpu, seqs, kv_heads=None):
                 scale=wl_gpu.scale, rows=rows)
 
 
-def oracle_pass(sample):
+def oracle_pass(sample, window=0):
     """One oracle step on a sample: its own KV write, then attention."""
     import oracle
     kc, vc = sample["k_cache"].copy(), sample["v_cache"].copy()
     oracle.write(sample["k_new"], sample["v_new"], sample["slots"], kc, vc)
     out, _ = oracle.attention(sample["q"], kc, vc, sample["bt"], sample["cl"], sample["qsl"],
-                              sample["scale"])
+                              sample["scale"], window=window)
     return out
 
 
-def sample_bytes(sample):
+def sample_bytes(sample, window=0):
     """Algorithmic bytes of one oracle pass over a sample (same accounting as
     algorithmic_bytes)."""
     e = sample["k_cache"].dtype.itemsize
     hkv, d = sample["k_cache"].shape[2], sample["k_cache"].shape[3]
     hq = sample["q"].shape[1]
-    keys = int(sample["cl"].sum())
+    cl = sample["cl"].astype(np.int64)
+    if window > 0:
+        qn = np.diff(sample["qsl"]).astype(np.int64)
+        cl = cl - np.maximum(0, cl - qn - window + 1)
+    keys = int(cl.sum())
     t = int(sample["qsl"][-1])
     return keys * hkv * d * e * 2 + 2 * t * hq * d * e + 4 * t * hkv * d * e
 
 
-def cpu_baseline(samples, name, num_seqs, budget_s=12.0):
+def cpu_baseline(samples, name, num_seqs, window=0, budget_s=12.0):
     """The oracle, as it stands, over pre-step samples of the workload (one
     sequence each, all heads) until about budget_s of CPU time is spent."""
     import oracle
@@ -234,9 +240,9 @@ def cpu_baseline(samples, name, num_seqs, budget_s=12.0):
     while spent < budget_s:
         for smp in samples:
             t0 = time.perf_counter()
-            oracle_pass(smp)
+            oracle_pass(smp, window)
             spent += time.perf_counter() - t0
-            nbytes += sample_bytes(smp)
+            nbytes += sample_bytes(smp, window)
         passes += 1
     return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s",
             "cores": oracle.max_threads(), "kind": "oracle",
@@ -257,12 +263,12 @@ def run_pkv(args, rank, world, device):
                     num_seqs=args.num_seqs)
     if args.profile:
         return profile_only(args, wl)
-    attn_b, write_b, kv_b = algorithmic_bytes(wl)
+    attn_b, write_b, kv_b = algorithmic_bytes(wl, args.window)
     step_b = attn_b + write_b
     out = torch.empty_like(wl.q)
     meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, max_query_len=wl.max_query_len,
                          max_context_len=wl.max_context_len, num_decode_seqs=wl.num_decode_seqs,
-                         kv_split_tokens=args.kv_split)
+                         kv_split_tokens=args.kv_split, sliding_window=args.window)
     ws_n = pkv.workspace_size(wl.k_cache, meta)
     ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
@@ -277,7 +283,8 @@ def run_pkv(args, rank, world, device):
         base_samples = [oracle_sample(wl, [int(s)]) for s in perm]
 
     def step():
-        pkv.run_step(wl, out, workspace=ws, kv_split_tokens=args.kv_split, stream=stream)
+        pkv.run_step(wl, out, workspace=ws, kv_split_tokens=args.kv_split,
+                     sliding_window=args.window, stream=stream)
 
     pkv.get_error(clear=True)
     for _ in range(args.warmup):
@@ -305,7 +312,8 @@ def run_pkv(args, rank, world, device):
         pkv.attention(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
                       wl.query_start_loc, wl.scale, max_query_len=wl.max_query_len,
                       max_context_len=wl.max_context_len, num_decode_seqs=wl.num_decode_seqs,
-                      kv_split_tokens=args.kv_split, workspace=ws, stream=stream)
+                      kv_split_tokens=args.kv_split, sliding_window=args.window,
+                      workspace=ws, stream=stream)
         e2.record(stream)
     end.record(stream)
     torch.cuda.synchronize(device)
@@ -318,7 +326,7 @@ def run_pkv(args, rank, world, device):
     if pkv.get_error(clear=True):
         raise RuntimeError("device error word set during the timed region")
     # parity spot check on the timed output: a few rows against the oracle
-    parity = spot_check(wl, out, spot)
+    parity = spot_check(wl, out, spot, args.window)
 
     total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / args.steps
@@ -353,6 +361,7 @@ def run_pkv(args, rank, world, device):
                             f"(mean {wl.ctx_lens.mean():.0f})",
             "max_query_len": wl.max_query_len, "num_tokens": wl.num_tokens,
             "kv_split_tokens": args.kv_split or "auto",
+            "sliding_window": args.window or None,
             "step": "pkv_write of the new tokens + pkv_attention",
             "l2": f"inputs larger than L2: {kv_b / 1e9:.2f} GB of K/V read per step, no flush",
             "parallelism": f"replicas x{world} (independent sequence batches)",
@@ -374,7 +383,7 @@ def run_pkv(args, rank, world, device):
         "parity_max_abs_err": parity,
     }
     if base_samples:
-        line["cpu_baseline"] = cpu_baseline(base_samples, wl.name, wl.num_seqs)
+        line["cpu_baseline"] = cpu_baseline(base_samples, wl.name, wl.num_seqs, args.window)
     return line
 
 
@@ -393,10 +402,10 @@ def profile_only(args, wl):
     return None
 
 
-def spot_check(wl, out, spot):
+def spot_check(wl, out, spot, window=0):
     """Max |error| of the timed output rows of the spot sample against the
     oracle (run on the pre-step copy)."""
-    exp = oracle_pass(spot)
+    exp = oracle_pass(spot, window)
     got = out[torch.tensor(spot["rows"], device=out.device)].float().cpu().numpy()
     err = float(np.abs(got.astype(np.float64) - exp).max())
     if not (err <= (2e-2 if wl.dtype == torch.bfloat16 else 1e-5)):
@@ -417,7 +426,8 @@ def end_to_end(wl, args, stream, device, step_bytes):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
     meta_kw = dict(max_query_len=wl.max_query_len, max_context_len=wl.max_context_len,
-                   num_decode_seqs=wl.num_decode_seqs, kv_split_tokens=args.kv_split)
+                   num_decode_seqs=wl.num_decode_seqs, kv_split_tokens=args.kv_split,
+                   sliding_window=args.window)
     meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **meta_kw)
     ws = torch.empty(max(pkv.workspace_size(wl.k_cache, meta), 1), dtype=torch.uint8,
                      device=device)
@@ -505,6 +515,8 @@ def main():
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--kv-split", type=int, default=0)
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window W (keys per query); 0 = full attention")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="override the batch size (profiling captures on a smaller case)")

@@ -98,6 +98,11 @@ typedef struct {
                               /* PKV_ERR_CONTEXT_LEN (rows zero)                */
   int32_t num_decode_seqs;    /* sequences 0..n-1 have query length 1 (the      */
                               /* decode run of a mixed batch); -1 = unknown     */
+  int32_t sliding_window;     /* W > 0: query at position pos sees only keys    */
+                              /* pos - W < p <= pos ([book] ch. 6 causal window */
+                              /* (w, 0), ch. 2 sliding_window); block-table     */
+                              /* entries before that range are never read, so   */
+                              /* they may hold the null block.  0 = no window   */
   int32_t kv_split_tokens;    /* split-K chunk in keys for decode: 0 = choose   */
                               /* automatically, else a multiple of 64 in        */
                               /* [64, 2048]                                     */

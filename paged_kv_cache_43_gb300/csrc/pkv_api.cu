@@ -132,6 +132,7 @@ int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan
   if (m->num_q_heads < 1 || m->num_q_heads % c->num_kv_heads != 0) return PKV_E_GQA;
   if (m->num_q_heads > 65535) return PKV_E_SHAPE;
   if (m->num_decode_seqs < -1 || m->num_decode_seqs > m->num_seqs) return PKV_E_META;
+  if (m->sliding_window < 0) return PKV_E_META;
   if (m->kv_split_tokens != 0 &&
       (m->kv_split_tokens < 64 || m->kv_split_tokens > 2048 || m->kv_split_tokens % 64 != 0))
     return PKV_E_META;
@@ -142,7 +143,13 @@ int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan
   else if (m->num_decode_seqs >= 0) nd = m->num_decode_seqs;
   p->num_decode = nd;
   if (nd == 0) return PKV_OK;
-  const int max_blocks = (m->max_context_len + kBlock - 1) / kBlock;
+  // Blocks a decode query may read: the whole context, or the window's span
+  // (which can straddle one block boundary more than W / 16 blocks do).
+  int max_blocks = (m->max_context_len + kBlock - 1) / kBlock;
+  if (m->sliding_window > 0) {
+    const int wb = (m->sliding_window + kBlock - 1) / kBlock + 1;
+    if (wb < max_blocks) max_blocks = wb;
+  }
   int split_blocks;
   if (m->kv_split_tokens > 0) {
     split_blocks = m->kv_split_tokens / kBlock;
@@ -158,7 +165,7 @@ int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan
     const int64_t slots = 2LL * num_sms;  // two CTAs per SM
     auto ctas = [&](int sb) { return units * ((max_blocks + sb - 1) / sb); };
     split_blocks = 64;
-    if (m->max_context_len >= 16384 && ctas(128) >= 4 * slots) split_blocks = 128;
+    if (max_blocks * kBlock >= 16384 && ctas(128) >= 4 * slots) split_blocks = 128;
     while (split_blocks > 4 && ctas(split_blocks) < 2 * slots) split_blocks /= 2;
   }
   p->split_blocks = split_blocks;
@@ -257,6 +264,7 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
     a.num_kv_heads = cache->num_kv_heads;
     a.head_size = cache->head_size;
     a.num_blocks = cache->num_blocks;
+    a.window = meta->sliding_window;
     a.scale = scale;
     return launch_attention_f32(a, st) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
   }
@@ -288,6 +296,7 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
     d.max_splits = p.max_splits;
     d.num_tokens = meta->num_tokens;
     d.max_context_len = meta->max_context_len;
+    d.window = meta->sliding_window;
     d.scale_log2 = scale * LOG2E;
     if (launch_decode_bf16(kmap, vmap, d, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
     if (launch_combine_bf16(d, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
@@ -310,6 +319,7 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
     f.num_blocks = cache->num_blocks;
     f.num_tokens = meta->num_tokens;
     f.max_query_len = meta->max_query_len;
+    f.window = meta->sliding_window;
     f.scale_log2 = scale * LOG2E;
     if (prefill_tc_supported(cache->head_size, G)) {
       // tcgen05/TMEM kernel: two tiles of 128/G tokens x G heads per CTA.

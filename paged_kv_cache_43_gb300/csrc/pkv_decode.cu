@@ -92,11 +92,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
     return;
   }
-  const int nblk_seq = (L + kBlock - 1) / kBlock;
+  // Keys the query sees: [kfirst, L) (the sliding window, if any); the splits
+  // cover the blocks of that range only.
+  const int kfirst = (a.window > 0 && L > a.window) ? L - a.window : 0;
+  const int blk0 = kfirst / kBlock;
+  const int nblk_seq = (L + kBlock - 1) / kBlock - blk0;
   const int nsplit = (nblk_seq + a.split_blocks - 1) / a.split_blocks;
   if (split >= nsplit) return;
-  const int b_begin = split * a.split_blocks;
-  const int b_end = min(b_begin + a.split_blocks, nblk_seq);
+  const int b_begin = blk0 + split * a.split_blocks;
+  const int b_end = min(b_begin + a.split_blocks, blk0 + nblk_seq);
   const int nblk = b_end - b_begin;
   const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;  // <= 32 by construction
 
@@ -199,8 +203,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         ldsm_x4(kbuf + swz_offset(k_row, kk * 16 + k_dsub), a0, a1, a2, a3);
         mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
       }
-      // ---- mask keys past the context (they may hold stale NaN)
-      const bool v0 = p0 + r0 < L, v1 = p0 + r0 + 8 < L;
+      // ---- mask keys past the context (they may hold stale NaN) and before
+      //      the window
+      const bool v0 = p0 + r0 < L && p0 + r0 >= kfirst;
+      const bool v1 = p0 + r0 + 8 < L && p0 + r0 + 8 >= kfirst;
       float x[4];
       x[0] = v0 ? sc[0] * a.scale_log2 : -INFINITY;
       x[1] = v0 ? sc[1] * a.scale_log2 : -INFINITY;
@@ -363,7 +369,9 @@ __global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs 
   if (qn != 1 || q0 < 0 || q0 >= a.num_tokens || L < 1 ||
       static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len)
     return;
-  const int nsplit = ((L + kBlock - 1) / kBlock + a.split_blocks - 1) / a.split_blocks;
+  const int kfirst = (a.window > 0 && L > a.window) ? L - a.window : 0;
+  const int nblk_seq = (L + kBlock - 1) / kBlock - kfirst / kBlock;
+  const int nsplit = (nblk_seq + a.split_blocks - 1) / a.split_blocks;
   if (nsplit <= 1) return;  // the decode kernel wrote this row directly
   const int64_t row = (static_cast<int64_t>(s) * a.num_q_heads + hq) * a.max_splits;
   const float* lse = a.ws_lse + row;

@@ -60,7 +60,8 @@ __global__ void __launch_bounds__(kF32Warps * 32) pkv_attention_f32_kernel(const
   }
   float m = -INFINITY, l = 0.f;
   const int32_t* bt = a.block_tables + static_cast<int64_t>(s) * a.bt_stride;
-  for (int p = warp; p <= pos; p += kF32Warps) {
+  const int kfirst = (a.window > 0 && pos + 1 > a.window) ? pos + 1 - a.window : 0;
+  for (int p = kfirst + warp; p <= pos; p += kF32Warps) {
     const int bid = __ldg(bt + p / kBlock);
     if (bid < 0 || bid >= a.num_blocks) {
       if (lane == 0) raise_error(a.err, PKV_ERR_BLOCK_ID);

@@ -45,6 +45,7 @@ struct DecodeArgs {
   int32_t max_splits;
   int32_t num_tokens;            // rows of q/out: query_start_loc must stay inside
   int32_t max_context_len;       // bound the split buffer was sized for
+  int32_t window;                // sliding window (keys per query), 0 = none
   float scale_log2;              // scale * log2(e)
 };
 
@@ -66,6 +67,7 @@ struct PrefillArgs {
   int32_t num_mtiles;            // grid.x: row tiles of the longest sequence
   int32_t num_tokens;
   int32_t max_query_len;
+  int32_t window;                // sliding window (keys per query), 0 = none
   float scale_log2;
 };
 
@@ -86,6 +88,7 @@ struct F32Args {
   int32_t num_kv_heads;
   int32_t head_size;
   int32_t num_blocks;
+  int32_t window;                // sliding window (keys per query), 0 = none
   float scale;
 };
 

@@ -93,6 +93,15 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   const int pos_max = L - qn + row_last / G;          // last key any row of this CTA sees
   const int ntiles = (pos_max + kTileKeys) / kTileKeys;
   const int nblk = (pos_max + kBlock) / kBlock;       // cache blocks to load
+  // With a sliding window, tiles wholly before the lowest row's window are
+  // never loaded (their block-table entries may hold the null block).
+  const int pos_min = L - qn + row0 / G;
+  const int j0 = (a.window > 0 && pos_min - a.window + 1 > 0)
+                     ? (pos_min - a.window + 1) / kTileKeys : 0;
+  // First cache block holding a key some row can see: earlier blocks of tile
+  // j0 are not loaded (their entries may be null); their V rows are zeroed.
+  const int b_lo = (a.window > 0 && pos_min - a.window + 1 > 0)
+                       ? (pos_min - a.window + 1) / kBlock : 0;
 
   if (threadIdx.x == 0) {
     prefetch_tensor_map(&kmap);
@@ -111,13 +120,14 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
     const uint64_t policy = policy_evict_first();
     const int32_t* bt = a.block_tables + static_cast<int64_t>(s) * a.bt_stride;
     int my_bid = -1;
-    for (int it = 0; it < ntiles; ++it) {
-      const int st = it % NS;
-      if (it >= NS && !mbar_wait(empty0 + 8 * st, ((it / NS) - 1) & 1)) {
+    for (int it = j0; it < ntiles; ++it) {
+      const int rel = it - j0;  // ring position
+      const int st = rel % NS;
+      if (rel >= NS && !mbar_wait(empty0 + 8 * st, ((rel / NS) - 1) & 1)) {
         if (lane == 0) raise_error(a.err, PKV_ERR_TIMEOUT);
         break;
       }
-      if ((it & 7) == 0) {  // block ids for the next 8 tiles, one per lane
+      if ((rel & 7) == 0) {  // block ids for the next 8 tiles, one per lane
         const int b = it * 4 + lane;
         my_bid = b < nblk ? __ldg(bt + b) : -1;
       }
@@ -126,8 +136,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
       uint32_t bytes = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        bid[b] = __shfl_sync(0xffffffffu, my_bid, (it & 7) * 4 + b);
-        const bool in_range = it * 4 + b < nblk;
+        bid[b] = __shfl_sync(0xffffffffu, my_bid, (rel & 7) * 4 + b);
+        const bool in_range = it * 4 + b < nblk && it * 4 + b >= b_lo;
         ok[b] = in_range && bid[b] >= 0 && bid[b] < a.num_blocks;
         if (in_range && !ok[b] && lane == 0) raise_error(a.err, PKV_ERR_BLOCK_ID);
         bytes += ok[b] ? 2u * T::kBlkBytes : 0u;
@@ -165,6 +175,9 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   const int jA = vA ? rA / G : qn - 1, jB = vB ? rB / G : qn - 1;
   const int posA = L - qn + jA, posB = L - qn + jB;
   const int wpos_min = L - qn + min(wrow0, nrows - 1) / G;
+  const int wpos_max = L - qn + min(wrow0 + 15, nrows - 1) / G;
+  const int W = a.window;
+  const int loA = W > 0 ? posA - W + 1 : 0, loB = W > 0 ? posB - W + 1 : 0;  // window starts
 
   // Q as the A operand: a0 = (rA, k), a1 = (rB, k), a2 = (rA, k+8), a3 = (rB, k+8)
   uint32_t qa[D / 16][4];
@@ -192,24 +205,29 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
   const int vb_key = (lane & 7) + ((lane >> 3) & 1) * 8;  // V (B operand, .trans)
   const int vb_d = (lane >> 4) * 8;
 
-  for (int it = 0; it < ntiles; ++it) {
-    const int st = it % NS;
-    if (!mbar_wait(full0 + 8 * st, (it / NS) & 1)) {
+  for (int it = j0; it < ntiles; ++it) {
+    const int st = (it - j0) % NS;
+    if (!mbar_wait(full0 + 8 * st, ((it - j0) / NS) & 1)) {
       if (lane == 0) raise_error(a.err, PKV_ERR_TIMEOUT);
       break;
     }
     const uint32_t kst = smem_u32(smem + st * T::kStageBytes);
     const uint32_t vst = kst + T::kKBytes;
     const int tile0 = it * kTileKeys;
-    if (it == ntiles - 1 && tile0 + kTileKeys > pos_max + 1) {
-      // Keys past pos_max have P = 0 for every row here, but their V rows may
-      // hold stale NaN (slots >= L) or whatever an earlier tile left (blocks
-      // not loaded): zero them so that 0 * NaN cannot reach the MMA.
-      const int first = pos_max + 1 - tile0;  // first key of the tile to clear (> 0)
+    const int lead = min(kTileKeys, b_lo * kBlock - tile0);      // keys not loaded (> 0 only at j0)
+    const int tail = (it == ntiles - 1) ? pos_max + 1 - tile0 : kTileKeys;  // first unseen key
+    if (lead > 0 || tail < kTileKeys) {
+      // Keys before the first loaded block or past pos_max have P = 0 for
+      // every row here, but their V rows may hold stale NaN (slots >= L) or
+      // whatever an earlier tile left (blocks not loaded): zero them so that
+      // 0 * NaN cannot reach the MMA.
       uint8_t* vrows = smem + st * T::kStageBytes + T::kKBytes;
       const int per_row = (D / 64) * 8;  // 16-byte chunks per key row
-      for (int e = threadIdx.x; e < (kTileKeys - first) * per_row; e += NWC * 32) {
-        const int key = first + e / per_row;
+      const int nlead = lead > 0 ? lead : 0;
+      const int ntail = kTileKeys - tail;
+      for (int e = threadIdx.x; e < (nlead + ntail) * per_row; e += NWC * 32) {
+        const int r = e / per_row;
+        const int key = r < nlead ? r : tail + (r - nlead);
         const int rem = e % per_row;
         *reinterpret_cast<uint4*>(vrows + (key >> 4) * T::kBlkBytes + (rem >> 3) * 2048 +
                                   (key & 15) * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -237,7 +255,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
       }
     }
     // ---- scale, causal mask, online softmax
-    const bool need_mask = tile0 + kTileKeys - 1 > wpos_min;
+    const bool need_mask = tile0 + kTileKeys - 1 > wpos_min || (W > 0 && tile0 <= wpos_max - W);
     float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
@@ -247,8 +265,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32)
         float xa = sc[nt][c] * a.scale_log2;
         float xb = sc[nt][2 + c] * a.scale_log2;
         if (need_mask) {
-          xa = (key + c <= posA) ? xa : -INFINITY;
-          xb = (key + c <= posB) ? xb : -INFINITY;
+          xa = (key + c <= posA && key + c >= loA) ? xa : -INFINITY;
+          xb = (key + c <= posB && key + c >= loB) ? xb : -INFINITY;
         }
         sc[nt][c] = xa;
         sc[nt][2 + c] = xb;

@@ -169,6 +169,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int ntq = (tok0 + tile_toks < qn) ? 2 : 1;  // query tiles holding a valid row
   const int pos_max = L - qn + tok_last;            // last key any row here can see
   const int ntiles = (pos_max + kTcKeys) / kTcKeys;
+  // With a sliding window, K/V tiles wholly before the lowest row's window
+  // are never loaded (their block-table entries may hold the null block): the
+  // CTA walks tiles j0 .. ntiles-1, ring positions 0 .. n_rel-1.
+  const int pos_min = L - qn + tok0;
+  const int j0 = (a.window > 0 && pos_min - a.window + 1 > 0)
+                     ? (pos_min - a.window + 1) / kTcKeys : 0;
+  const int n_rel = ntiles - j0;
+  // First cache block holding a key some row can see; blocks before it in
+  // tile j0 are not loaded (their entries may be null) and their V rows are
+  // zeroed instead.
+  const int lo_min = a.window > 0 ? pos_min - a.window + 1 : 0;
+  const int b_lo = lo_min > 0 ? lo_min / kBlock : 0;
   const int nblk = (pos_max + kBlock) / kBlock;
 
   const uint32_t q_full = smem_u32(&sh->q_full), drain = smem_u32(&sh->drain);
@@ -228,7 +240,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int b = 0; b < kBlocks; ++b) {
         bid[b] = __shfl_sync(0xffffffffu, ids, b);
-        const bool in_range = it * kBlocks + b < nblk;
+        const int blk = it * kBlocks + b;
+        const bool in_range = blk < nblk && blk >= b_lo;
         ok[b] = in_range && bid[b] >= 0 && bid[b] < a.num_blocks;
         if (!is_v && in_range && !ok[b] && lane == 0) raise_error(a.err, PKV_ERR_BLOCK_ID);
         bytes += ok[b] ? Lt::kHalves * 2048u : 0u;
@@ -249,22 +262,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     };
-    int ids_cur = load_ids(0), ids_prev = -1;
-    for (int it = 0; it <= ntiles; ++it) {
+    int ids_cur = load_ids(j0), ids_prev = -1;
+    for (int it = j0; it <= ntiles; ++it) {
       const int ids_next = load_ids(it + 1);
       if (it < ntiles) {
-        const int st = it % kKStages;
-        if (it >= kKStages &&
-            !warp_wait(smem_u32(&sh->k_empty[st]), ((it / kKStages) - 1) & 1, abort, a.err))
+        const int rel = it - j0;  // ring position of K tile `it`
+        const int st = rel % kKStages;
+        if (rel >= kKStages &&
+            !warp_wait(smem_u32(&sh->k_empty[st]), ((rel / kKStages) - 1) & 1, abort, a.err))
           break;
         issue_tile(it, ids_cur, false, smem_u32(sK + st * Lt::kTileBytes),
                    smem_u32(&sh->k_full[st]));
       }
-      if (it >= 1) {
+      if (it >= j0 + 1) {
         const int iv = it - 1;
-        const int st = iv % kVStages;
-        if (iv >= kVStages &&
-            !warp_wait(smem_u32(&sh->v_empty[st]), ((iv / kVStages) - 1) & 1, abort, a.err))
+        const int rv = iv - j0;   // ring position of V tile `iv`
+        const int st = rv % kVStages;
+        if (rv >= kVStages &&
+            !warp_wait(smem_u32(&sh->v_empty[st]), ((rv / kVStages) - 1) & 1, abort, a.err))
           break;
         issue_tile(iv, ids_prev, true, smem_u32(sV + st * Lt::kTileBytes),
                    smem_u32(&sh->v_full[st]));
@@ -327,7 +342,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // P_t(js - 1) V is enough; doing so at once makes the tensor-core
           // order P0 V, S0, P1 V, S1 and offsets the two softmaxes by half a
           // period, so one runs while the other tile's products do.
-          if (js < ntiles && pv_next[t] == js &&
+          if (js < n_rel && pv_next[t] == js &&
               mbar_test(smem_u32(&sh->k_full[js % kKStages]), (js / kKStages) & 1)) {
             tc::fence_after_sync();
             issue_s(t, js);
@@ -348,7 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::commit(smem_u32(&sh->v_empty[v_released % kVStages]));
           ++v_released;
         }
-        if (done_pv == ntiles) break;
+        if (done_pv == n_rel) break;
         if (progress) {
           idle_since = 0;
         } else {
@@ -387,7 +402,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool done = t < ntq;
-    for (int j = 0; done && j < ntiles; ++j) {
+    const int lo = a.window > 0 ? pos - a.window + 1 : 0;  // first key in this row's window
+    for (int j = 0; done && j < n_rel; ++j) {
       // S_t(j) complete (its commit also covers P_t(j - 1) V, so O_t is stable)
       if (!warp_wait(b_sfull, j & 1, abort, a.err)) { done = false; break; }
       tc::fence_after_sync();
@@ -402,10 +418,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::wait_ld();
       // causal mask on raw scores (also hides keys >= L); scale > 0, so the
       // row max of the raw scores gives the max of the scaled ones
-      const int key0 = j * kTcKeys;
-      if (key0 + kTcKeys - 1 > pos) {
+      const int key0 = (j0 + j) * kTcKeys;
+      if (key0 + kTcKeys - 1 > pos || key0 < lo) {
 #pragma unroll
-        for (int c = 0; c < kTcKeys; ++c) x[c] = (key0 + c > pos) ? -INFINITY : x[c];
+        for (int c = 0; c < kTcKeys; ++c)
+          x[c] = (key0 + c > pos || key0 + c < lo) ? -INFINITY : x[c];
       }
       // row max: four independent chains of three-input maxima
       float m4[4] = {x[0], x[1], x[2], x[3]};
@@ -458,19 +475,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float ls = (tc::sum_f32x2(acc[0]) + tc::sum_f32x2(acc[1])) +
                        (tc::sum_f32x2(acc[2]) + tc::sum_f32x2(acc[3]));
       l = l * alpha + ls;
-      if (j == ntiles - 1 && key0 + kTcKeys > pos_max + 1) {
-        // Keys past pos_max have P = 0 in every row, but their V rows may be
-        // stale NaN or left over from an earlier tile: zero them before this
-        // warpgroup's P V product may be issued.  Both warpgroups do it (the
-        // MMAs of the two query tiles are issued in either order); the
-        // second writes zeros over zeros.
+      const int lead = min(kTcKeys, b_lo * kBlock - key0);       // keys not loaded (> 0 only at j == 0)
+      const int tail = (j == n_rel - 1) ? pos_max + 1 - key0 : kTcKeys;  // keys from here on unseen
+      if (lead > 0 || tail < kTcKeys) {
+        // Keys before the first loaded block or past pos_max have P = 0 in
+        // every row, but their V rows may be stale NaN or left over from an
+        // earlier tile: zero them before this warpgroup's P V product may be
+        // issued.  Both warpgroups do it (the MMAs of the two query tiles are
+        // issued in either order); the second writes zeros over zeros.
         if (!warp_wait(smem_u32(&sh->v_full[j % kVStages]), (j / kVStages) & 1, abort,
                        a.err)) { done = false; break; }
         uint8_t* vt = sV + (j % kVStages) * Lt::kTileBytes;
-        const int first = pos_max + 1 - key0;
         const int per_row = Lt::kHalves * 8;
-        for (int e = ts; e < (kTcKeys - first) * per_row; e += 128) {
-          const int key = first + e / per_row;
+        const int nlead = lead > 0 ? lead : 0;
+        const int ntail = kTcKeys - tail;
+        for (int e = ts; e < (nlead + ntail) * per_row; e += 128) {
+          const int r = e / per_row;
+          const int key = r < nlead ? r : tail + (r - nlead);
           const int rem = e % per_row;
           *reinterpret_cast<uint4*>(vt + (rem >> 3) * Lt::kKvHalf + key * 128 + (rem & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
@@ -482,7 +503,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pfull);
     }
-    if (done && warp_wait(b_pvdone, (ntiles - 1) & 1, abort, a.err)) {
+    if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * D;

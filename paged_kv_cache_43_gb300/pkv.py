@@ -42,7 +42,8 @@ class AttnMeta(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
                 ("num_q_heads", ctypes.c_int32), ("block_table_stride", ctypes.c_int32),
                 ("max_query_len", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
-                ("num_decode_seqs", ctypes.c_int32), ("kv_split_tokens", ctypes.c_int32)]
+                ("num_decode_seqs", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
+                ("kv_split_tokens", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -132,10 +133,10 @@ def write(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
 
 
 def attn_meta(q, block_tables, context_lens, *, max_query_len, max_context_len,
-              num_decode_seqs=-1, kv_split_tokens=0) -> AttnMeta:
+              num_decode_seqs=-1, kv_split_tokens=0, sliding_window=0) -> AttnMeta:
     return AttnMeta(int(context_lens.shape[0]), int(q.shape[0]), int(q.shape[1]),
                     int(block_tables.shape[1]), int(max_query_len), int(max_context_len),
-                    int(num_decode_seqs), int(kv_split_tokens))
+                    int(num_decode_seqs), int(sliding_window), int(kv_split_tokens))
 
 
 def workspace_size(k_cache, meta: AttnMeta) -> int:
@@ -148,7 +149,7 @@ def workspace_size(k_cache, meta: AttnMeta) -> int:
 
 def attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
               *, max_query_len, max_context_len, num_decode_seqs=-1, kv_split_tokens=0,
-              workspace=None, stream=None) -> None:
+              sliding_window=0, workspace=None, stream=None) -> None:
     """pkv_attention into ``out`` [T, Hq, D].  ``workspace`` (uint8 CUDA tensor)
     is allocated here when not given and the batch needs split-K scratch."""
     lib = load()
@@ -161,7 +162,7 @@ def attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start_
         raise PkvError("out and q must have the same shape")
     meta = attn_meta(q, block_tables, context_lens, max_query_len=max_query_len,
                      max_context_len=max_context_len, num_decode_seqs=num_decode_seqs,
-                     kv_split_tokens=kv_split_tokens)
+                     kv_split_tokens=kv_split_tokens, sliding_window=sliding_window)
     desc = cache_desc(k_cache)
     need = workspace_size(k_cache, meta)
     if need and workspace is None:
@@ -177,7 +178,8 @@ def attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start_
 
 def attention_static_scratch(out, q, k_cache, v_cache, block_tables, context_lens,
                              query_start_loc, scale, *, max_query_len, max_context_len,
-                             num_decode_seqs=-1, kv_split_tokens=0, stream=None) -> int:
+                             num_decode_seqs=-1, kv_split_tokens=0, sliding_window=0,
+                             stream=None) -> int:
     """pkv_attention_static_scratch: pkv_attention with the split-K workspace
     taken from the library's own fixed device array (no allocation anywhere).
     Returns the C status (0 = enqueued; PKV_E_WORKSPACE = batch needs more than
@@ -190,7 +192,7 @@ def attention_static_scratch(out, q, k_cache, v_cache, block_tables, context_len
     _require(query_start_loc, "query_start_loc", dtype=torch.int32, ndim=1)
     meta = attn_meta(q, block_tables, context_lens, max_query_len=max_query_len,
                      max_context_len=max_context_len, num_decode_seqs=num_decode_seqs,
-                     kv_split_tokens=kv_split_tokens)
+                     kv_split_tokens=kv_split_tokens, sliding_window=sliding_window)
     desc = cache_desc(k_cache)
     return int(lib.pkv_attention_static_scratch(
         out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
@@ -209,11 +211,12 @@ def status_string(status: int) -> str:
     return load().pkv_status_string(status).decode()
 
 
-def run_step(wl, out, workspace=None, kv_split_tokens=0, stream=None) -> None:
+def run_step(wl, out, workspace=None, kv_split_tokens=0, sliding_window=0, stream=None) -> None:
     """One pass of the hot path over a workload: the KV write of this step's
     tokens, then attention over the updated cache."""
     write(wl.k_new, wl.v_new, wl.slot_mapping, wl.k_cache, wl.v_cache, stream=stream)
     attention(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
               wl.query_start_loc, wl.scale, max_query_len=wl.max_query_len,
               max_context_len=wl.max_context_len, num_decode_seqs=wl.num_decode_seqs,
-              kv_split_tokens=kv_split_tokens, workspace=workspace, stream=stream)
+              kv_split_tokens=kv_split_tokens, sliding_window=sliding_window,
+              workspace=workspace, stream=stream)

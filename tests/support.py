@@ -12,7 +12,7 @@ from paged_kv_cache_43_gb300 import workloads as W
 TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2}
 
 
-def oracle_step(wl):
+def oracle_step(wl, window=0):
     """Oracle result of one step on a CPU workload: (out fp64, status, k_cache,
     v_cache) after the oracle's own write of this step's tokens."""
     A = W.as_oracle_array
@@ -20,7 +20,7 @@ def oracle_step(wl):
     bad = oracle.write(A(wl.k_new), A(wl.v_new), A(wl.slot_mapping), kc, vc)
     assert bad == 0
     out, st = oracle.attention(A(wl.q), kc, vc, A(wl.block_tables), A(wl.context_lens),
-                               A(wl.query_start_loc), wl.scale)
+                               A(wl.query_start_loc), wl.scale, window=window)
     return out, st, kc, vc
 
 
@@ -44,7 +44,7 @@ def nan_like(t: torch.Tensor) -> torch.Tensor:
     return torch.full_like(t, float("nan"))
 
 
-def compact_subproblem(wl_gpu, seqs, pre_k, pre_v):
+def compact_subproblem(wl_gpu, seqs, pre_k, pre_v, window=0):
     """CPU oracle inputs for the sequences `seqs` of a GPU workload: their
     blocks gathered (from the pre-write pools pre_k/pre_v) into a compact pool,
     block tables renumbered, the oracle's own write of their new tokens
@@ -83,5 +83,5 @@ def compact_subproblem(wl_gpu, seqs, pre_k, pre_v):
     sub_slots = np.array([remap[int(b)] * W.BLOCK_SIZE + int(o) for b, o in zip(blk, off)],
                          np.int64)
     assert oracle.write(kn, vn, sub_slots, kc, vc) == 0
-    P = oracle.Problem(q, kc, vc, sub_bt, sub_cl, sub_qsl, wl_gpu.scale)
+    P = oracle.Problem(q, kc, vc, sub_bt, sub_cl, sub_qsl, wl_gpu.scale, window)
     return P, rows
