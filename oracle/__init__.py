@@ -34,7 +34,7 @@ _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16 = 0, 1
+F32, BF16, FP8 = 0, 1, 2
 
 
 class OrcProblem(ctypes.Structure):
@@ -55,6 +55,8 @@ class OrcProblem(ctypes.Structure):
         ("dtype", ctypes.c_int32),
         ("scale", ctypes.c_double),
         ("window", ctypes.c_int32),
+        ("k_descale", ctypes.c_void_p),
+        ("v_descale", ctypes.c_void_p),
     ]
 
 
@@ -94,6 +96,15 @@ def _load():
         lib.orc_attention.restype = ctypes.c_int32
         lib.orc_attention.argtypes = [ctypes.POINTER(OrcProblem), ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_int32]
+        lib.orc_e4m3_decode.restype = ctypes.c_double
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_write_fp8.restype = ctypes.c_int64
+        lib.orc_write_fp8.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
         lib.orc_max_threads.restype = ctypes.c_int32
         lib.orc_max_threads.argtypes = []
         _lib = lib
@@ -111,12 +122,39 @@ def _ptr(a: np.ndarray) -> int:
 
 def dtype_code(arr: np.ndarray) -> int:
     """Storage code of a cache/query array: float32 -> F32, uint16 (bf16 bit
-    patterns) -> BF16."""
+    patterns) -> BF16, uint8 (e4m3 codes) -> FP8."""
     if arr.dtype == np.float32:
         return F32
     if arr.dtype == np.uint16:
         return BF16
+    if arr.dtype == np.uint8:
+        return FP8
     raise TypeError(f"oracle takes float32 or uint16 (bf16 bits), got {arr.dtype}")
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one e4m3 code (FP8 KV cache, ch. 6 capability matrix)."""
+    return float(_load().orc_e4m3_decode(int(code)))
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest e4m3 code of an fp32 value (ties to even, clamped to 448)."""
+    return int(_load().orc_e4m3_encode(float(x)))
+
+
+def write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale) -> int:
+    """FP8 KV write: k/v bf16 bits (uint16) [T, Hkv, D] quantised to e4m3 codes
+    with per-kv-head scales (encode(k / scale) in fp32) into uint8 caches
+    [NB, bs, Hkv, D], in place.  Returns the number of out-of-range slots."""
+    lib = _load()
+    k, v = _raw(np.asarray(k, np.uint16)), _raw(np.asarray(v, np.uint16))
+    slots = _raw(np.asarray(slot_mapping, dtype=np.int64))
+    ks = _raw(np.asarray(k_scale, np.float32))
+    vs = _raw(np.asarray(v_scale, np.float32))
+    assert k_cache.dtype == np.uint8 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    nb, bs, hkv, d = k_cache.shape
+    return int(lib.orc_write_fp8(_ptr(k), _ptr(v), _ptr(slots), slots.shape[0], _ptr(k_cache),
+                                 _ptr(v_cache), nb, bs, hkv, d, _ptr(ks), _ptr(vs)))
 
 
 def write(k, v, slot_mapping, k_cache, v_cache) -> int:
@@ -139,15 +177,20 @@ class Problem:
     """Keeps the numpy buffers of one attention problem alive for ctypes."""
 
     def __init__(self, q, k_cache, v_cache, block_tables, context_lens,
-                 query_start_loc, scale, window: int = 0):
+                 query_start_loc, scale, window: int = 0, k_descale=None, v_descale=None):
         self.q = _raw(q)
         self.k_cache = _raw(k_cache)
         self.v_cache = _raw(v_cache)
         self.block_tables = _raw(np.asarray(block_tables, dtype=np.int32))
         self.context_lens = _raw(np.asarray(context_lens, dtype=np.int32))
         self.query_start_loc = _raw(np.asarray(query_start_loc, dtype=np.int32))
-        code = dtype_code(self.q)
-        assert dtype_code(self.k_cache) == code == dtype_code(self.v_cache)
+        code = dtype_code(self.k_cache)
+        assert code == dtype_code(self.v_cache)
+        assert dtype_code(self.q) == (BF16 if code == FP8 else code)
+        self.k_descale = self.v_descale = None
+        if code == FP8:
+            self.k_descale = _raw(np.asarray(k_descale, np.float32))
+            self.v_descale = _raw(np.asarray(v_descale, np.float32))
         nb, bs, hkv, d = self.k_cache.shape
         self.num_tokens, hq, dq = self.q.shape
         assert dq == d and hq % hkv == 0
@@ -158,20 +201,25 @@ class Problem:
             _ptr(self.q), _ptr(self.k_cache), _ptr(self.v_cache),
             _ptr(self.block_tables), _ptr(self.context_lens), _ptr(self.query_start_loc),
             self.block_tables.shape[1] if self.block_tables.ndim == 2 else 0,
-            s, hq, hkv, d, bs, nb, code, float(scale), int(window))
+            s, hq, hkv, d, bs, nb, code, float(scale), int(window),
+            _ptr(self.k_descale) if self.k_descale is not None else None,
+            _ptr(self.v_descale) if self.v_descale is not None else None)
 
 
 def attention(q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
-              scale, nthreads: int = 0, window: int = 0):
+              scale, nthreads: int = 0, window: int = 0, k_descale=None, v_descale=None):
     """Exact paged attention in fp64 (ch. 6 "Structure des métadonnées",
     "Flux des paramètres du chemin non-cascadé", "Branche de masque"); with
     ``window`` W > 0 a query at position pos sees keys pos - W < p <= pos.
+    With uint8 (e4m3) caches, q is bf16 and K/V are decode(code) times
+    ``k_descale`` / ``v_descale`` [num_seqs, num_kv_heads].
 
     Returns ``(out, seq_status)``: ``out`` is float64 [T, Hq, D]; rows of a
     sequence with status 1 (metadata error) are zero, status 2 (block id out of
     range) NaN."""
     lib = _load()
-    P = Problem(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, window)
+    P = Problem(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale, window,
+                k_descale, v_descale)
     out = np.zeros((P.num_tokens, P.shape["Hq"], P.shape["D"]), dtype=np.float64)
     status = np.zeros(P.shape["S"], dtype=np.int32)
     lib.orc_attention(ctypes.byref(P.c), _ptr(out), _ptr(status), int(nthreads))

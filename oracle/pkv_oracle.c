@@ -40,6 +40,15 @@
  *    itself); block-table entries wholly before that range are never read (they
  *    may hold the null block).  W = 0 means no window.
  *
+ *  - FP8 KV cache ([book] ch. 6 "Matrice de capacités": fp8 cache dtypes;
+ *    "Flux des paramètres": descales shaped (num_sequences, num_kv_heads)):
+ *    the cache holds e4m3 codes (sign, 4 exponent bits with bias 7, 3 mantissa
+ *    bits; exponent 0 is subnormal; S.1111.111 is NaN; no infinities; largest
+ *    finite 448).  Writing stores encode(k / k_scale[h]) with the division in
+ *    fp32, rounding to the nearest code (ties to the even code) and clamping
+ *    magnitudes above 448 to 448.  Attention reads K = decode(code) *
+ *    k_descale[s][h] and V = decode(code) * v_descale[s][h].
+ *
  *  - Partial state and merge (the split buffer of [book] ch. 6 "build() étape
  *    par étape", fourth step, and merge_attn_states in the ch. 6 sequence
  *    diagram): a key range yields (m, l, acc) = (max x, sum e^(x-m),
@@ -59,7 +68,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8 = 2 };
 
 typedef struct {
   const void *q;              /* [num_tokens, num_q_heads, head_size] */
@@ -73,12 +82,45 @@ typedef struct {
   int32_t dtype;              /* ORC_F32 or ORC_BF16 */
   double scale;
   int32_t window;             /* sliding window W (keys per query), 0 = none */
+  const float *k_descale;     /* ORC_FP8 caches: [num_seqs, num_kv_heads] */
+  const float *v_descale;
 } orc_problem;
+
+/* e4m3 code -> value, straight from the format's definition. */
+double orc_e4m3_decode(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m / 8.0, -6);          /* subnormal */
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* value -> e4m3 code: the nearest of the 127 finite magnitudes (ties to the
+ * code with an even last bit), sign kept (so -0 stays -0), magnitudes above
+ * 448 clamped to 448, NaN to 0x7F.  A plain search over every code. */
+uint8_t orc_e4m3_encode(float x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs((double)x);
+  if (a > 448.0) a = 448.0;
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    const double err = fabs(orc_e4m3_decode((uint8_t)c) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
 
 /* One stored element, widened exactly to double.  bf16 is the top half of an
  * IEEE binary32, so shifting its 16 bits up and reinterpreting is exact. */
 static double orc_load(const void *base, int64_t idx, int32_t dtype) {
   float f;
+  if (dtype == ORC_FP8) return orc_e4m3_decode(((const uint8_t *)base)[idx]);
   if (dtype == ORC_F32) {
     memcpy(&f, (const char *)base + idx * 4, 4);
   } else {
@@ -107,6 +149,34 @@ int64_t orc_write(const void *k, const void *v, const int64_t *slot_mapping,
     const int64_t dst = (blk * block_size + off) * row;
     memcpy((char *)k_cache + dst, (const char *)k + t * row, (size_t)row);
     memcpy((char *)v_cache + dst, (const char *)v + t * row, (size_t)row);
+  }
+  return bad;
+}
+
+/* FP8 KV write: every element of row t of k/v (bf16 bits) divided in fp32 by
+ * its kv head's scale and encoded; rows with slot < 0 skipped.  Returns the
+ * number of out-of-range slots. */
+int64_t orc_write_fp8(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
+                      int64_t num_tokens, uint8_t *k_cache, uint8_t *v_cache,
+                      int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                      int32_t head_size, const float *k_scale, const float *v_scale) {
+  const int64_t row = (int64_t)num_kv_heads * head_size;
+  int64_t bad = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_blocks * block_size) { ++bad; continue; }
+    for (int64_t i = 0; i < row; ++i) {
+      const int32_t h = (int32_t)(i / head_size);
+      uint32_t uk = ((uint32_t)k[t * row + i]) << 16, uv = ((uint32_t)v[t * row + i]) << 16;
+      float fk, fv;
+      memcpy(&fk, &uk, 4);
+      memcpy(&fv, &uv, 4);
+      const float qk = fk / k_scale[h];   /* fp32 division, round to nearest */
+      const float qv = fv / v_scale[h];
+      k_cache[slot * row + i] = orc_e4m3_encode(qk);
+      v_cache[slot * row + i] = orc_e4m3_encode(qv);
+    }
   }
   return bad;
 }
@@ -148,6 +218,10 @@ int orc_row_state(const orc_problem *P, int32_t s, int32_t hq, int32_t j,
 
   const int64_t t = P->query_start_loc[s] + j;
   const int64_t qbase = (t * P->num_q_heads + hq) * D;
+  /* q is bf16 when the cache is fp8 */
+  const int32_t qtype = P->dtype == ORC_FP8 ? ORC_BF16 : P->dtype;
+  const double kd = P->dtype == ORC_FP8 ? (double)P->k_descale[(int64_t)s * Hkv + kvh] : 1.0;
+  const double vd = P->dtype == ORC_FP8 ? (double)P->v_descale[(int64_t)s * Hkv + kvh] : 1.0;
   double *x = (double *)malloc(sizeof(double) * (size_t)(hi - lo));
   int64_t *row = (int64_t *)malloc(sizeof(int64_t) * (size_t)(hi - lo));
   int status = 0;
@@ -159,7 +233,7 @@ int orc_row_state(const orc_problem *P, int32_t s, int32_t hq, int32_t j,
     const int64_t kbase = (slot * Hkv + kvh) * D;
     double dot = 0.0;
     for (int32_t d = 0; d < D; ++d)
-      dot += orc_load(P->q, qbase + d, P->dtype) * orc_load(P->k_cache, kbase + d, P->dtype);
+      dot += orc_load(P->q, qbase + d, qtype) * (orc_load(P->k_cache, kbase + d, P->dtype) * kd);
     x[p - lo] = P->scale * dot;
     row[p - lo] = kbase;
     if (x[p - lo] > m) m = x[p - lo];
@@ -169,7 +243,8 @@ int orc_row_state(const orc_problem *P, int32_t s, int32_t hq, int32_t j,
     for (int64_t p = lo; p < hi; ++p) {
       const double w = exp(x[p - lo] - m);
       l += w;
-      for (int32_t d = 0; d < D; ++d) acc[d] += w * orc_load(P->v_cache, row[p - lo] + d, P->dtype);
+      for (int32_t d = 0; d < D; ++d)
+        acc[d] += w * (orc_load(P->v_cache, row[p - lo] + d, P->dtype) * vd);
     }
     *m_out = m;
     *l_out = l;

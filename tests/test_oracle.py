@@ -387,3 +387,88 @@ def test_window_never_reads_blocks_before_the_window():
     out2, st = oracle.attention(q, kc, vc, bt2, cl, qsl, sc, window=20)
     assert not st.any()
     np.testing.assert_array_equal(out, out2)
+
+
+# ------------------------------------------------------------ FP8 (e4m3) cache
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).float().double().numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all() and nan.sum() == 2          # 0x7F, 0xFF
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_rounding_in_range():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.normal(0, 1, 4000), rng.normal(0, 100, 2000),
+                        rng.uniform(-2 ** -6, 2 ** -6, 2000),             # subnormal range
+                        [1.0625, 1.1875, 2 ** -10, 3 * 2 ** -10, -0.0, 440.0, 447.9]])
+    x = np.clip(x, -448, 448).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(v) for v in x], dtype=np.uint8)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_e4m3_encode_clamps_beyond_the_largest_finite():
+    assert oracle.e4m3_encode(448.0) == 0x7E
+    assert oracle.e4m3_encode(1e6) == 0x7E and oracle.e4m3_encode(-500.0) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def test_fp8_write_quantises_per_head_and_skips_padding():
+    wl = W.make_workload([1, 3], [20, 35], num_q_heads=4, num_kv_heads=2, head_size=64,
+                         dtype=torch.bfloat16, seed=31)
+    A = W.as_oracle_array
+    nb = wl.num_blocks
+    kc = np.full((nb, 16, 2, 64), 0x7F, np.uint8)
+    vc = kc.copy()
+    slots = A(wl.slot_mapping).copy()
+    slots[0] = -1
+    ks = np.array([0.5, 2.0], np.float32)
+    vs = np.array([1.25, 0.125], np.float32)
+    assert oracle.write_fp8(A(wl.k_new), A(wl.v_new), slots, kc, vc, ks, vs) == 0
+    # expectation built with torch: fp32 division by the head's scale, then
+    # torch's e4m3 cast (values here stay inside +-448)
+    for t in range(len(slots)):
+        if slots[t] < 0:
+            continue
+        for cache, src, sc in ((kc, wl.k_new, ks), (vc, wl.v_new, vs)):
+            x = src[t].float() / torch.from_numpy(sc)[:, None]
+            assert float(x.abs().max()) <= 448
+            ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            np.testing.assert_array_equal(cache.reshape(-1, 2, 64)[slots[t]], ref)
+    assert (kc.reshape(-1, 2, 64)[A(wl.slot_mapping)[0]] == 0x7F).all()   # padding skipped
+
+
+def test_fp8_attention_equals_bf16_attention_on_representable_values():
+    """Codes times power-of-two descales are exact in bf16: the fp8 path must
+    give the bf16 path's result."""
+    wl = W.make_workload([1, 6, 1], [45, 70, 33], num_q_heads=8, num_kv_heads=2,
+                         head_size=64, dtype=torch.bfloat16, seed=32)
+    A = W.as_oracle_array
+    rng = np.random.default_rng(1)
+    nb = wl.num_blocks
+    codes_k = rng.integers(0, 0x7E, size=(nb, 16, 2, 64), dtype=np.uint8) | \
+        (rng.integers(0, 2, size=(nb, 16, 2, 64), dtype=np.uint8) << 7)
+    codes_v = rng.integers(0, 0x7E, size=(nb, 16, 2, 64), dtype=np.uint8)
+    kd = np.array([[2.0 ** -6, 2.0 ** -5], [2.0 ** -7, 2.0 ** -6], [2.0 ** -5, 2.0 ** -8]],
+                  np.float32)
+    vd = np.array([[0.5, 0.25], [1.0, 0.5], [0.125, 1.0]], np.float32)
+    dec = np.vectorize(oracle.e4m3_decode)
+    kval, vval = dec(codes_k), dec(codes_v)
+    out8, st = oracle.attention(A(wl.q), codes_k, codes_v, A(wl.block_tables),
+                                A(wl.context_lens), A(wl.query_start_loc), wl.scale,
+                                k_descale=kd, v_descale=vd)
+    assert not st.any()
+    # same values as bf16 caches, sequence by sequence (descales differ per sequence)
+    for s in range(3):
+        k16 = torch.from_numpy(kval * kd[s][None, None, :, None]).to(torch.bfloat16)
+        v16 = torch.from_numpy(vval * vd[s][None, None, :, None]).to(torch.bfloat16)
+        assert torch.equal(k16.double(), torch.from_numpy(kval * kd[s][None, None, :, None]))
+        ref, _ = oracle.attention(A(wl.q), A(k16), A(v16), A(wl.block_tables),
+                                  A(wl.context_lens), A(wl.query_start_loc), wl.scale)
+        q0, q1 = int(wl.query_start_loc[s]), int(wl.query_start_loc[s + 1])
+        np.testing.assert_allclose(out8[q0:q1], ref[q0:q1], atol=1e-12, rtol=0)
