@@ -100,21 +100,27 @@ def recorded_traffic(workload_name: str):
     return rec.get("per_workload", {}).get(workload_name)
 
 
-def algorithmic_bytes(wl, window=0):
+def algorithmic_bytes(wl, window=0, fp8=False):
     """Bytes the step must move at minimum.
-    attention: each K and V row some query of its sequence can see, once; q
-    read, out written, the block-table entries of those rows and per-sequence
-    metadata read; write: new K/V rows read and written, slots read."""
+    attention: each K and V row some query of its sequence can see, once (one
+    byte per element for an e4m3 cache); q read, out written, the block-table
+    entries of those rows and per-sequence metadata (and descales) read;
+    write: new K/V rows read and written (as codes for e4m3), slots read."""
     e = wl.q.element_size()
+    ekv = 1 if fp8 else e
     hkv, d, hq = wl.num_kv_heads, wl.head_size, wl.num_q_heads
     ctx = wl.ctx_lens.astype(np.int64)
     if window > 0:   # keys [L - q_s - W + 1, L) are visible to some row
         ctx = ctx - np.maximum(0, ctx - wl.q_lens.astype(np.int64) - window + 1)
-    kv = int(ctx.sum()) * hkv * d * e * 2
+    kv = int(ctx.sum()) * hkv * d * ekv * 2
     qo = 2 * wl.num_tokens * hq * d * e
     meta = int(np.ceil(ctx / 16).sum()) * 4 + wl.num_seqs * 4 + (wl.num_seqs + 1) * 4
+    if fp8:
+        meta += 2 * wl.num_seqs * hkv * 4
     attn = kv + qo + meta
-    write = 2 * 2 * wl.num_tokens * hkv * d * e + wl.num_tokens * 8
+    write = 2 * wl.num_tokens * hkv * d * (e + ekv) + wl.num_tokens * 8
+    if fp8:
+        write += 2 * hkv * 4
     return attn, write, kv
 
 
@@ -172,11 +178,13 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- oracle leg
 
-def oracle_sample(wl_gpu, seqs, kv_heads=None):
+def oracle_sample(wl_gpu, seqs, kv_heads=None, fp8=None):
     """CPU inputs (compact pool) for the sequences `seqs`, with this step's new
     tokens, for the oracle.  Must be taken before any step has run, so that
     no oracle input passes through the CUDA path.  `kv_heads` keeps only the
-    first kv heads (and their query-head groups)."""
+    first kv heads (and their query-head groups).  `fp8` = (k_scale, v_scale,
+    k_descale, v_descale) as numpy: the sample's history is quantised to e4m3
+    by the oracle (every other slot holds the NaN code)."""
     from paged_kv_cache_43_gb300 import workloads as W
     bt = wl_gpu.block_tables.cpu().numpy()
     cl = wl_gpu.context_lens.cpu().numpy()
@@ -199,18 +207,42 @@ def oracle_sample(wl_gpu, seqs, kv_heads=None):
     slots = wl_gpu.slot_mapping.cpu().numpy()[rows]
     sub_slots = np.array([remap[int(x) // 16] * 16 + int(x) % 16 for x in slots], np.int64)
     A = W.as_oracle_array
-    return dict(q=A(wl_gpu.q.index_select(0, rows_t)[:, : hkv * g]),
-                k_new=A(wl_gpu.k_new.index_select(0, rows_t)[:, :hkv]),
-                v_new=A(wl_gpu.v_new.index_select(0, rows_t)[:, :hkv]),
-                slots=sub_slots, k_cache=kc, v_cache=vc, bt=sub_bt,
-                cl=cl[seqs].astype(np.int32), qsl=np.array(sub_qsl, np.int32),
-                scale=wl_gpu.scale, rows=rows)
+    smp = dict(q=A(wl_gpu.q.index_select(0, rows_t)[:, : hkv * g]),
+               k_new=A(wl_gpu.k_new.index_select(0, rows_t)[:, :hkv]),
+               v_new=A(wl_gpu.v_new.index_select(0, rows_t)[:, :hkv]),
+               slots=sub_slots, k_cache=kc, v_cache=vc, bt=sub_bt,
+               cl=cl[seqs].astype(np.int32), qsl=np.array(sub_qsl, np.int32),
+               scale=wl_gpu.scale, rows=rows)
+    if fp8 is not None:
+        import oracle
+        ks, vs, kd, vd = (np.ascontiguousarray(a) for a in fp8)
+        ks, vs = ks[:hkv].copy(), vs[:hkv].copy()
+        kd, vd = kd[seqs][:, :hkv].copy(), vd[seqs][:, :hkv].copy()
+        hist = []
+        for i, s in enumerate(seqs):
+            pos = np.arange(int(cl[s]) - int(qsl[s + 1] - qsl[s]))
+            hist.append(sub_bt[i, pos // 16].astype(np.int64) * 16 + pos % 16)
+        hist = np.unique(np.concatenate(hist))
+        d = kc.shape[3]
+        k8 = np.full(kc.shape, W.E4M3_NAN_CODE, np.uint8)
+        v8 = k8.copy()
+        assert oracle.write_fp8(kc.reshape(-1, hkv, d)[hist], vc.reshape(-1, hkv, d)[hist],
+                                hist, k8, v8, ks, vs) == 0
+        smp.update(k_cache=k8, v_cache=v8, fp8=(ks, vs, kd, vd))
+    return smp
 
 
 def oracle_pass(sample, window=0):
     """One oracle step on a sample: its own KV write, then attention."""
     import oracle
     kc, vc = sample["k_cache"].copy(), sample["v_cache"].copy()
+    if "fp8" in sample:
+        ks, vs, kd, vd = sample["fp8"]
+        oracle.write_fp8(sample["k_new"], sample["v_new"], sample["slots"], kc, vc, ks, vs)
+        out, _ = oracle.attention(sample["q"], kc, vc, sample["bt"], sample["cl"],
+                                  sample["qsl"], sample["scale"], window=window,
+                                  k_descale=kd, v_descale=vd)
+        return out
     oracle.write(sample["k_new"], sample["v_new"], sample["slots"], kc, vc)
     out, _ = oracle.attention(sample["q"], kc, vc, sample["bt"], sample["cl"], sample["qsl"],
                               sample["scale"], window=window)
@@ -220,7 +252,8 @@ def oracle_pass(sample, window=0):
 def sample_bytes(sample, window=0):
     """Algorithmic bytes of one oracle pass over a sample (same accounting as
     algorithmic_bytes)."""
-    e = sample["k_cache"].dtype.itemsize
+    ekv = sample["k_cache"].dtype.itemsize
+    e = sample["q"].dtype.itemsize
     hkv, d = sample["k_cache"].shape[2], sample["k_cache"].shape[3]
     hq = sample["q"].shape[1]
     cl = sample["cl"].astype(np.int64)
@@ -229,7 +262,7 @@ def sample_bytes(sample, window=0):
         cl = cl - np.maximum(0, cl - qn - window + 1)
     keys = int(cl.sum())
     t = int(sample["qsl"][-1])
-    return keys * hkv * d * e * 2 + 2 * t * hq * d * e + 4 * t * hkv * d * e
+    return keys * hkv * d * ekv * 2 + 2 * t * hq * d * e + 2 * t * hkv * d * (e + ekv)
 
 
 def cpu_baseline(samples, name, num_seqs, window=0, budget_s=12.0):
@@ -253,38 +286,97 @@ def cpu_baseline(samples, name, num_seqs, window=0, budget_s=12.0):
 
 # ----------------------------------------------------------------- arms
 
+class KVCache:
+    """The caches a step runs on and the two calls of the step.  bf16: the
+    workload's own pool.  fp8: e4m3 pools whose history is quantised from the
+    workload's bf16 pool by pkv_write_fp8 (setup, not timed), per-kv-head
+    scales drawn from the workload's seed; every sequence reads with the
+    scales its blocks were written with."""
+
+    def __init__(self, wl, fp8, seed, kv_split, window):
+        from paged_kv_cache_43_gb300 import pkv
+        from paged_kv_cache_43_gb300 import workloads as W
+        self.pkv, self.wl, self.fp8 = pkv, wl, fp8
+        self.meta_kw = dict(max_query_len=wl.max_query_len, max_context_len=wl.max_context_len,
+                            num_decode_seqs=wl.num_decode_seqs, kv_split_tokens=kv_split,
+                            sliding_window=window)
+        dev = wl.q.device
+        if not fp8:
+            self.k, self.v = wl.k_cache, wl.v_cache
+            self.np_scales = None
+            return
+        ks = W.fp8_scales(wl.num_kv_heads, seed)
+        vs = W.fp8_scales(wl.num_kv_heads, seed + 1)
+        kd, vd = np.tile(ks, (wl.num_seqs, 1)), np.tile(vs, (wl.num_seqs, 1))
+        self.np_scales = (ks, vs, kd, vd)
+        self.ks, self.vs, self.kd, self.vd = (torch.from_numpy(a).to(dev)
+                                              for a in self.np_scales)
+        self.k = torch.full(wl.k_cache.shape, W.E4M3_NAN_CODE, dtype=torch.uint8, device=dev)
+        self.v = torch.full_like(self.k, W.E4M3_NAN_CODE)
+        nb, bs, hkv, d = wl.k_cache.shape
+        slots = torch.from_numpy(W.history_slots(wl)).to(dev)
+        for part in torch.split(slots, 1 << 20):
+            pkv.write_fp8(wl.k_cache.view(-1, hkv, d).index_select(0, part),
+                          wl.v_cache.view(-1, hkv, d).index_select(0, part), part,
+                          self.k, self.v, self.ks, self.vs)
+        torch.cuda.synchronize(dev)
+
+    def write(self, k_new, v_new, slots, stream):
+        if self.fp8:
+            self.pkv.write_fp8(k_new, v_new, slots, self.k, self.v, self.ks, self.vs,
+                               stream=stream)
+        else:
+            self.pkv.write(k_new, v_new, slots, self.k, self.v, stream=stream)
+
+    def attention(self, out, q, bt, cl, qsl, ws, stream, kd=None, vd=None):
+        if self.fp8:
+            self.pkv.attention_fp8(out, q, self.k, self.v, bt, cl, qsl, self.wl.scale,
+                                   self.kd if kd is None else kd, self.vd if vd is None else vd,
+                                   workspace=ws, stream=stream, **self.meta_kw)
+        else:
+            self.pkv.attention(out, q, self.k, self.v, bt, cl, qsl, self.wl.scale,
+                               workspace=ws, stream=stream, **self.meta_kw)
+
+    def step(self, out, ws, stream):
+        wl = self.wl
+        self.write(wl.k_new, wl.v_new, wl.slot_mapping, stream)
+        self.attention(out, wl.q, wl.block_tables, wl.context_lens, wl.query_start_loc, ws,
+                       stream)
+
+
 def run_pkv(args, rank, world, device):
     from paged_kv_cache_43_gb300 import build, pkv
     from paged_kv_cache_43_gb300 import workloads as W
 
     build.build()
     pkv.load()
-    wl = W.workload(args.workload, device=device, seed=rank_seed(args.workload, rank),
-                    num_seqs=args.num_seqs)
+    seed = rank_seed(args.workload, rank)
+    wl = W.workload(args.workload, device=device, seed=seed, num_seqs=args.num_seqs)
+    fp8 = args.kv_dtype == "fp8"
+    kv = KVCache(wl, fp8, seed, args.kv_split, args.window)
     if args.profile:
-        return profile_only(args, wl)
-    attn_b, write_b, kv_b = algorithmic_bytes(wl, args.window)
+        return profile_only(args, kv)
+    attn_b, write_b, kv_b = algorithmic_bytes(wl, args.window, fp8)
     step_b = attn_b + write_b
     out = torch.empty_like(wl.q)
-    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, max_query_len=wl.max_query_len,
-                         max_context_len=wl.max_context_len, num_decode_seqs=wl.num_decode_seqs,
-                         kv_split_tokens=args.kv_split, sliding_window=args.window)
-    ws_n = pkv.workspace_size(wl.k_cache, meta)
+    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **kv.meta_kw)
+    ws_n = pkv.workspace_size(kv.k, meta)
     ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     nd = wl.num_seqs if wl.max_query_len <= 1 else wl.num_decode_seqs
     launches_per_step = (1 + (1 if nd > 0 else 0) + (1 if ws_n else 0)
                          + (1 if nd < wl.num_seqs else 0))
-    # Oracle inputs are copied from the pristine (pre-step) cache.
-    spot = oracle_sample(wl, [int(np.argmin(wl.ctx_lens)), int(np.argmax(wl.ctx_lens))])
+    # Oracle inputs are copied from the pristine (pre-step) bf16 pool; for fp8
+    # the oracle quantises them itself.
+    spot = oracle_sample(wl, [int(np.argmin(wl.ctx_lens)), int(np.argmax(wl.ctx_lens))],
+                         fp8=kv.np_scales)
     base_samples = []
     if rank == 0 and not args.no_cpu_baseline:
         perm = np.random.default_rng(0).permutation(wl.num_seqs)[:12]
-        base_samples = [oracle_sample(wl, [int(s)]) for s in perm]
+        base_samples = [oracle_sample(wl, [int(s)], fp8=kv.np_scales) for s in perm]
 
     def step():
-        pkv.run_step(wl, out, workspace=ws, kv_split_tokens=args.kv_split,
-                     sliding_window=args.window, stream=stream)
+        kv.step(out, ws, stream)
 
     pkv.get_error(clear=True)
     for _ in range(args.warmup):
@@ -307,13 +399,9 @@ def run_pkv(args, rank, world, device):
     for i in range(args.steps):
         e0, e1, e2 = ev[i]
         e0.record(stream)
-        pkv.write(wl.k_new, wl.v_new, wl.slot_mapping, wl.k_cache, wl.v_cache, stream=stream)
+        kv.write(wl.k_new, wl.v_new, wl.slot_mapping, stream)
         e1.record(stream)
-        pkv.attention(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
-                      wl.query_start_loc, wl.scale, max_query_len=wl.max_query_len,
-                      max_context_len=wl.max_context_len, num_decode_seqs=wl.num_decode_seqs,
-                      kv_split_tokens=args.kv_split, sliding_window=args.window,
-                      workspace=ws, stream=stream)
+        kv.attention(out, wl.q, wl.block_tables, wl.context_lens, wl.query_start_loc, ws, stream)
         e2.record(stream)
     end.record(stream)
     torch.cuda.synchronize(device)
@@ -332,14 +420,14 @@ def run_pkv(args, rank, world, device):
     ms_per_step = total_ms / args.steps
 
     # ---- end to end: host buffers in, host result out, same stream
-    e2e = end_to_end(wl, args, stream, device, step_b)
+    e2e = end_to_end(kv, args, stream, device, step_b)
 
     if rank != 0:
         return None
     peak, peak_kind = hbm_peak()
     value = job_throughput(step_b, world, ms_per_step)
     achieved = attn_b / (attn_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name)
+    traffic = recorded_traffic(wl.name + ("-fp8" if fp8 else ""))
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -362,7 +450,10 @@ def run_pkv(args, rank, world, device):
             "max_query_len": wl.max_query_len, "num_tokens": wl.num_tokens,
             "kv_split_tokens": args.kv_split or "auto",
             "sliding_window": args.window or None,
-            "step": "pkv_write of the new tokens + pkv_attention",
+            "kv_cache_dtype": "fp8_e4m3" if fp8 else ("bf16" if wl.dtype == torch.bfloat16
+                                                       else "f32"),
+            "step": ("pkv_write_fp8 of the new tokens + pkv_attention_fp8" if fp8 else
+                     "pkv_write of the new tokens + pkv_attention"),
             "l2": f"inputs larger than L2: {kv_b / 1e9:.2f} GB of K/V read per step, no flush",
             "parallelism": f"replicas x{world} (independent sequence batches)",
         },
@@ -387,18 +478,23 @@ def run_pkv(args, rank, world, device):
     return line
 
 
-def profile_only(args, wl):
+def profile_only(args, kv):
     """Warm-up then `steps` plain steps, nothing else: a short, fixed launch
     sequence for ncu captures (not a bench measurement)."""
     from paged_kv_cache_43_gb300 import pkv
+    wl = kv.wl
     out = torch.empty_like(wl.q)
+    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **kv.meta_kw)
+    ws = torch.empty(max(pkv.workspace_size(kv.k, meta), 1), dtype=torch.uint8,
+                     device=wl.q.device)
+    stream = torch.cuda.current_stream()
     for _ in range(args.warmup + args.steps):
-        pkv.run_step(wl, out, kv_split_tokens=args.kv_split)
+        kv.step(out, ws, stream)
     torch.cuda.synchronize()
     if pkv.get_error(clear=True):
         raise RuntimeError("device error word set")
-    print(json.dumps({"profile_run": wl.name, "num_seqs": wl.num_seqs,
-                      "steps": args.warmup + args.steps}), flush=True)
+    print(json.dumps({"profile_run": wl.name, "kv_cache_dtype": args.kv_dtype,
+                      "num_seqs": wl.num_seqs, "steps": args.warmup + args.steps}), flush=True)
     return None
 
 
@@ -413,34 +509,35 @@ def spot_check(wl, out, spot, window=0):
     return err
 
 
-def end_to_end(wl, args, stream, device, step_bytes):
+def end_to_end(kv, args, stream, device, step_bytes):
     """Same metric through the public calls with host-resident step inputs:
-    pinned H2D of q, new K/V, slots and metadata, the step, D2H of out."""
+    pinned H2D of q, new K/V, slots and metadata (and the descales of an e4m3
+    cache), the step, D2H of out."""
     from paged_kv_cache_43_gb300 import pkv
+    wl = kv.wl
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
              "query_start_loc")
-    host = {n: getattr(wl, n).cpu().pin_memory() for n in names}
-    dev = {n: torch.empty_like(getattr(wl, n)) for n in names}
+    src = {n: getattr(wl, n) for n in names}
+    if kv.fp8:
+        src.update(k_descale=kv.kd, v_descale=kv.vd)
+    host = {n: t.cpu().pin_memory() for n, t in src.items()}
+    dev = {n: torch.empty_like(t) for n, t in src.items()}
     out_h = torch.empty(wl.q.shape, dtype=wl.q.dtype).pin_memory()
     out_d = torch.empty_like(wl.q)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
-    meta_kw = dict(max_query_len=wl.max_query_len, max_context_len=wl.max_context_len,
-                   num_decode_seqs=wl.num_decode_seqs, kv_split_tokens=args.kv_split,
-                   sliding_window=args.window)
-    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **meta_kw)
-    ws = torch.empty(max(pkv.workspace_size(wl.k_cache, meta), 1), dtype=torch.uint8,
+    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **kv.meta_kw)
+    ws = torch.empty(max(pkv.workspace_size(kv.k, meta), 1), dtype=torch.uint8,
                      device=device)
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            for n in names:
+            for n in host:
                 dev[n].copy_(host[n], non_blocking=True)
-        pkv.write(dev["k_new"], dev["v_new"], dev["slot_mapping"], wl.k_cache, wl.v_cache,
-                  stream=stream)
-        pkv.attention(out_d, dev["q"], wl.k_cache, wl.v_cache, dev["block_tables"],
-                      dev["context_lens"], dev["query_start_loc"], wl.scale, stream=stream,
-                      workspace=ws, **meta_kw)
+        kv.write(dev["k_new"], dev["v_new"], dev["slot_mapping"], stream)
+        kv.attention(out_d, dev["q"], dev["block_tables"], dev["context_lens"],
+                     dev["query_start_loc"], ws, stream, kd=dev.get("k_descale"),
+                     vd=dev.get("v_descale"))
         with torch.cuda.stream(stream):
             out_h.copy_(out_d, non_blocking=True)
 
@@ -475,7 +572,12 @@ def run_reference(args, rank, world):
     wl = W.workload(args.workload, device=device)
     budget = float(os.environ.get("PKV_REFERENCE_BUDGET_S", "150"))
     seq = int(np.argsort(wl.ctx_lens)[wl.num_seqs // 2])      # median-length sequence
-    smp = oracle_sample(wl, [seq])
+    scales = None
+    if args.kv_dtype == "fp8":    # same scales as the pkv arm's rank 0
+        sd = rank_seed(args.workload, 0)
+        ks, vs = W.fp8_scales(wl.num_kv_heads, sd), W.fp8_scales(wl.num_kv_heads, sd + 1)
+        scales = (ks, vs, np.tile(ks, (wl.num_seqs, 1)), np.tile(vs, (wl.num_seqs, 1)))
+    smp = oracle_sample(wl, [seq], fp8=scales)
     t0 = time.perf_counter()
     oracle_pass(smp)
     one = time.perf_counter() - t0
@@ -483,7 +585,7 @@ def run_reference(args, rank, world):
     hkv = wl.num_kv_heads
     if one > per_step:
         hkv = max(1, int(wl.num_kv_heads * per_step / one))
-        smp = oracle_sample(wl, [seq], kv_heads=hkv)
+        smp = oracle_sample(wl, [seq], kv_heads=hkv, fp8=scales)
     for _ in range(args.warmup):
         oracle_pass(smp)
     t0 = time.perf_counter()
@@ -492,7 +594,8 @@ def run_reference(args, rank, world):
     dt = time.perf_counter() - t0
     value = sample_bytes(smp) * args.steps / dt / 1e9
     sample = (f"sequence {seq} of {wl.name} ({int(smp['cl'][0])} keys), {hkv} of "
-              f"{wl.num_kv_heads} kv heads with their q heads, fp64 KV write + attention")
+              f"{wl.num_kv_heads} kv heads with their q heads, fp64 KV write + attention"
+              + (" over an e4m3 cache" if scales is not None else ""))
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -517,6 +620,9 @@ def main():
     ap.add_argument("--kv-split", type=int, default=0)
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window W (keys per query); 0 = full attention")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="cache storage: the workload's bf16, or e4m3 codes with per-kv-head "
+                         "scales (workloads 2-5)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="override the batch size (profiling captures on a smaller case)")
@@ -525,6 +631,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.kv_dtype == "fp8" and args.workload == 1:
+        ap.error("--kv-dtype fp8 needs a bf16 workload (2-5)")
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local = _env_int("LOCAL_RANK", 0)

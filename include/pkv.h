@@ -46,7 +46,7 @@ extern "C" {
 /* ---- status codes (return values) -------------------------------------- */
 #define PKV_OK 0
 #define PKV_E_NULL (-1)        /* a required pointer is NULL                     */
-#define PKV_E_DTYPE (-2)       /* dtype not PKV_F32 / PKV_BF16                   */
+#define PKV_E_DTYPE (-2)       /* dtype not supported by this call               */
 #define PKV_E_SHAPE (-3)       /* unsupported head_size / block_size, or a size  */
                                /* is negative or too large                       */
 #define PKV_E_GQA (-4)         /* num_q_heads not a multiple of num_kv_heads     */
@@ -65,14 +65,16 @@ extern "C" {
                                      /* query length is not 1                    */
 #define PKV_ERR_TIMEOUT (1 << 5)     /* an on-chip wait gave up (bounded spin)   */
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 
 /* Shape of the paged KV cache ([book] ch. 6 "Transformation de la disposition
  * mémoire du KV cache": separate K and V caches, each
  * [num_blocks, block_size, num_kv_heads, head_size]).  One block of both
  * caches takes 2 * block_size * num_kv_heads * head_size * dtype_bytes bytes
  * ([gpuhub] note under "KV cache manager").
- * Supported: block_size 16, head_size 64 or 128, dtype PKV_BF16 or PKV_F32. */
+ * Supported: block_size 16, head_size 64 or 128, dtype PKV_BF16, PKV_F32 or
+ * PKV_FP8_E4M3 (e4m3 codes; [book] ch. 6 "Matrice de capacités": fp8 cache
+ * dtypes), the last through pkv_write_fp8 / pkv_attention_fp8 only. */
 typedef struct {
   int32_t num_blocks;
   int32_t block_size;
@@ -123,6 +125,19 @@ typedef struct {
 int pkv_write(const void *k, const void *v, const int64_t *slot_mapping,
               int32_t num_tokens, void *k_cache, void *v_cache,
               const pkv_cache_desc *cache, void *stream);
+
+/* FP8 KV-cache write: as pkv_write, but k and v are bf16 and each element is
+ * stored as the e4m3 code of k / k_scale[h] (v / v_scale[h]), h its kv head:
+ * the quotient is an fp32 division rounded to nearest, then rounded to the
+ * nearest e4m3 value (ties to the even code), magnitudes above 448 clamped to
+ * 448; a NaN input gives a NaN code.
+ *   k, v              bf16 [num_tokens, num_kv_heads, head_size]
+ *   k_cache, v_cache  uint8 e4m3 [num_blocks, block_size, num_kv_heads, head_size]
+ *   k_scale, v_scale  fp32 [num_kv_heads] (device)
+ * cache->dtype must be PKV_FP8_E4M3. */
+int pkv_write_fp8(const void *k, const void *v, const int64_t *slot_mapping,
+                  int32_t num_tokens, void *k_cache, void *v_cache, const float *k_scale,
+                  const float *v_scale, const pkv_cache_desc *cache, void *stream);
 
 /* Bytes of scratch workspace pkv_attention needs for this batch shape (the
  * split buffer of [book] ch. 6 "build() étape par étape", fourth step: one
@@ -197,6 +212,21 @@ int pkv_attention_static_scratch(void *out, const void *q, const void *k_cache,
                                  const int32_t *query_start_loc, float scale,
                                  const pkv_cache_desc *cache,
                                  const pkv_attn_meta *meta, void *stream);
+
+/* PagedAttention over an FP8 (e4m3) cache: as pkv_attention with q and out in
+ * bf16, and K = code value * k_descale[s][h], V = code value * v_descale[s][h]
+ * for sequence s, kv head h ([book] ch. 6 "Flux des paramètres du chemin
+ * non-cascadé": descales shaped (num_sequences, num_kv_heads)).  For the
+ * result to be the attention of the written K/V, k_descale[s][h] must equal
+ * the k_scale the blocks were written with (likewise for V).
+ *   k_descale, v_descale  fp32 [num_seqs, num_kv_heads] (device)
+ * Workspace as for pkv_attention (same size function). */
+int pkv_attention_fp8(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      const int32_t *query_start_loc, float scale, const float *k_descale,
+                      const float *v_descale, const pkv_cache_desc *cache,
+                      const pkv_attn_meta *meta, void *workspace, size_t workspace_bytes,
+                      void *stream);
 
 /* Reads (and, if clear != 0, resets) the current device's error word: the OR
  * of PKV_ERR_* bits raised by kernels since the last clear.  SYNCHRONISES the

@@ -58,23 +58,40 @@ int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return PKV_OK;
 }
 
-// TMA descriptor of one bf16 cache viewed as a 3-D tensor
-// (head_size, num_kv_heads, num_blocks * 16) with a box of 64 columns x 1 head
-// x 16 rows (one cache block of one head, 128 bytes wide) and the 128-byte
-// swizzle.
+// TMA descriptor of one cache viewed as a 3-D tensor
+// (head_size, num_kv_heads, num_blocks * 16).  bf16: a box of 64 columns x 1
+// head x 16 rows (one cache block of one head, 128 bytes wide) with the
+// 128-byte swizzle.  FP8 (e4m3 codes as bytes): a box of the whole head row x
+// 1 head x 16 rows with the swizzle of the row's width (128 or 64 bytes), which
+// keeps the kernels' per-lane fragment reads free of bank conflicts.
+// The L2 fill size is capped at one head row (64, 128 or 256 bytes): a wider
+// fill would pull the neighbouring kv head's row, which another CTA reads at
+// some other time, and double the DRAM traffic of narrow rows.
 int encode_cache_map(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
   PFN_cuTensorMapEncodeTiled_v12000 fn;
   if (int st = encode_fn(&fn)) return st;
+  const bool fp8 = c.dtype == PKV_FP8_E4M3;
+  const cuuint64_t eb = fp8 ? 1 : 2;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(c.head_size) * eb;
+  const CUtensorMapL2promotion promo =
+      row_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                       : (row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                           : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c.head_size),
                               static_cast<cuuint64_t>(c.num_kv_heads),
                               static_cast<cuuint64_t>(c.num_blocks) * c.block_size};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.head_size) * 2,
-                                 static_cast<cuuint64_t>(c.num_kv_heads) * c.head_size * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(c.block_size)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.head_size) * eb,
+                                 static_cast<cuuint64_t>(c.num_kv_heads) * c.head_size * eb};
+  const cuuint32_t box[3] = {fp8 ? static_cast<cuuint32_t>(c.head_size) : 64u, 1,
+                             static_cast<cuuint32_t>(c.block_size)};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  (fp8 && row_bytes == 64) ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_128B,
+                  promo,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PKV_OK : PKV_E_CUDA;
 }
 
@@ -103,7 +120,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int check_cache(const pkv_cache_desc* c) {
   if (c == nullptr) return PKV_E_NULL;
-  if (c->dtype != PKV_F32 && c->dtype != PKV_BF16) return PKV_E_DTYPE;
+  if (c->dtype != PKV_F32 && c->dtype != PKV_BF16 && c->dtype != PKV_FP8_E4M3) return PKV_E_DTYPE;
   if (c->block_size != kBlock) return PKV_E_SHAPE;
   if (c->head_size != 64 && c->head_size != 128) return PKV_E_SHAPE;
   if (c->num_kv_heads < 1 || c->num_blocks < 0) return PKV_E_SHAPE;
@@ -180,6 +197,13 @@ int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+int attention_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, const int32_t* context_lens,
+                   const int32_t* query_start_loc, float scale, const float* k_descale,
+                   const float* v_descale, const pkv_cache_desc* cache,
+                   const pkv_attn_meta* meta, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
 }  // namespace
 }  // namespace pkv
 
@@ -189,6 +213,7 @@ extern "C" int pkv_write(const void* k, const void* v, const int64_t* slot_mappi
                          int32_t num_tokens, void* k_cache, void* v_cache,
                          const pkv_cache_desc* cache, void* stream) {
   if (int st = check_cache(cache)) return st;
+  if (cache->dtype == PKV_FP8_E4M3) return PKV_E_DTYPE;  // pkv_write_fp8
   if (num_tokens < 0) return PKV_E_SHAPE;
   if (num_tokens == 0) return PKV_OK;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_E_NULL;
@@ -209,7 +234,42 @@ extern "C" int pkv_write(const void* k, const void* v, const int64_t* slot_mappi
   a.num_slots = static_cast<int64_t>(cache->num_blocks) * cache->block_size;
   a.num_tokens = num_tokens;
   a.row_vecs = cache->num_kv_heads * cache->head_size * ebytes / 16;
+  a.k_scale = a.v_scale = nullptr;
+  a.head_size = cache->head_size;
   return launch_write(a, as_stream(stream), sms) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
+}
+
+extern "C" int pkv_write_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                             int32_t num_tokens, void* k_cache, void* v_cache,
+                             const float* k_scale, const float* v_scale,
+                             const pkv_cache_desc* cache, void* stream) {
+  if (int st = check_cache(cache)) return st;
+  if (cache->dtype != PKV_FP8_E4M3) return PKV_E_DTYPE;
+  if (num_tokens < 0) return PKV_E_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return PKV_E_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return PKV_E_ALIGN;
+  int32_t* err;
+  int sms;
+  if (int st = device_state(&err, &sms)) return st;
+  WriteArgs a;
+  a.k = k;
+  a.v = v;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.err = err;
+  a.num_slots = static_cast<int64_t>(cache->num_blocks) * cache->block_size;
+  a.num_tokens = num_tokens;
+  a.row_vecs = cache->num_kv_heads * cache->head_size / 16;  // 16 codes per vector
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.head_size = cache->head_size;
+  return launch_write_fp8(a, as_stream(stream), sms) == cudaSuccess ? PKV_OK : PKV_E_CUDA;
 }
 
 extern "C" size_t pkv_attention_workspace_size(const pkv_cache_desc* cache,
@@ -227,6 +287,39 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
                              const int32_t* query_start_loc, float scale,
                              const pkv_cache_desc* cache, const pkv_attn_meta* meta,
                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (cache != nullptr && cache->dtype == PKV_FP8_E4M3) return PKV_E_DTYPE;  // pkv_attention_fp8
+  return attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                        scale, nullptr, nullptr, cache, meta, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pkv_attention_fp8(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, const int32_t* query_start_loc,
+                                 float scale, const float* k_descale, const float* v_descale,
+                                 const pkv_cache_desc* cache, const pkv_attn_meta* meta,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (cache == nullptr) return PKV_E_NULL;
+  if (cache->dtype != PKV_FP8_E4M3) return PKV_E_DTYPE;
+  if (meta != nullptr && meta->num_seqs > 0 && meta->num_tokens > 0) {
+    if (!k_descale || !v_descale) return PKV_E_NULL;
+    if ((reinterpret_cast<uintptr_t>(k_descale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_descale) & 3u))
+      return PKV_E_ALIGN;
+  }
+  return attention_impl(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                        scale, k_descale, v_descale, cache, meta, workspace, workspace_bytes,
+                        stream);
+}
+
+namespace pkv {
+namespace {
+
+int attention_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, const int32_t* context_lens,
+                   const int32_t* query_start_loc, float scale, const float* k_descale,
+                   const float* v_descale, const pkv_cache_desc* cache,
+                   const pkv_attn_meta* meta, void* workspace, size_t workspace_bytes,
+                   void* stream) {
   int32_t* err;
   int sms;
   if (int st = device_state(&err, &sms)) return st;
@@ -270,6 +363,7 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
   }
 
   if (cache->num_blocks == 0) return PKV_E_SHAPE;
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
   CUtensorMap kmap, vmap;
   if (int e = encode_cache_map(&kmap, k_cache, *cache)) return e;
   if (int e = encode_cache_map(&vmap, v_cache, *cache)) return e;
@@ -297,8 +391,11 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
     d.num_tokens = meta->num_tokens;
     d.max_context_len = meta->max_context_len;
     d.window = meta->sliding_window;
+    d.k_descale = k_descale;
+    d.v_descale = v_descale;
     d.scale_log2 = scale * LOG2E;
-    if (launch_decode_bf16(kmap, vmap, d, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
+    if (launch_decode_bf16(kmap, vmap, d, cache->head_size, fp8, st) != cudaSuccess)
+      return PKV_E_CUDA;
     if (launch_combine_bf16(d, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
   }
   const int npf = meta->num_seqs - p.num_decode;
@@ -320,8 +417,10 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
     f.num_tokens = meta->num_tokens;
     f.max_query_len = meta->max_query_len;
     f.window = meta->sliding_window;
+    f.k_descale = k_descale;
+    f.v_descale = v_descale;
     f.scale_log2 = scale * LOG2E;
-    if (prefill_tc_supported(cache->head_size, G)) {
+    if (!fp8 && prefill_tc_supported(cache->head_size, G)) {
       // tcgen05/TMEM kernel: two tiles of 128/G tokens x G heads per CTA.
       const int toks = prefill_tc_tokens_per_cta(G);
       f.num_mtiles = (meta->max_query_len + toks - 1) / toks;
@@ -332,15 +431,19 @@ extern "C" int pkv_attention(void* out, const void* q, const void* k_cache, cons
       if (launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, st) != cudaSuccess)
         return PKV_E_CUDA;
     } else {
-      // Group sizes that do not divide 128 rows: mma.sync kernel, 64 rows per CTA.
+      // FP8 caches, and group sizes that do not divide 128 rows: mma.sync
+      // kernel, 64 rows per CTA.
       const int64_t rows = static_cast<int64_t>(meta->max_query_len) * G;
       f.num_mtiles = static_cast<int32_t>((rows + kPrefillRows - 1) / kPrefillRows);
-      if (launch_prefill_bf16(kmap, vmap, f, cache->head_size, st) != cudaSuccess)
+      if (launch_prefill_bf16(kmap, vmap, f, cache->head_size, fp8, st) != cudaSuccess)
         return PKV_E_CUDA;
     }
   }
   return PKV_OK;
 }
+
+}  // namespace
+}  // namespace pkv
 
 extern "C" int pkv_get_error(int32_t* error_bits, int clear) {
   if (error_bits == nullptr) return PKV_E_NULL;
@@ -359,7 +462,9 @@ extern "C" const char* pkv_status_string(int status) {
   switch (status) {
     case PKV_OK: return "ok";
     case PKV_E_NULL: return "a required pointer is NULL";
-    case PKV_E_DTYPE: return "unsupported dtype (PKV_F32 or PKV_BF16)";
+    case PKV_E_DTYPE:
+      return "dtype not supported by this call (PKV_F32/PKV_BF16: pkv_write, pkv_attention; "
+             "PKV_FP8_E4M3: pkv_write_fp8, pkv_attention_fp8)";
     case PKV_E_SHAPE: return "unsupported or out-of-range shape (block_size 16, head_size 64/128)";
     case PKV_E_GQA: return "num_q_heads is not a multiple of num_kv_heads";
     case PKV_E_WORKSPACE: return "workspace missing or smaller than pkv_attention_workspace_size";

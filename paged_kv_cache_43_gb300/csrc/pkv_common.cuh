@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -171,6 +172,94 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// ---- fp16 operands (the FP8-cache kernels: every e4m3 value is exact in fp16)
+
+// D (16x8 fp32) += A (16x16 f16, row) * B (16x8 f16, col).
+__device__ __forceinline__ void mma_f16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t x) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t x) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16)));
+}
+
+// Four e4m3 codes (byte i = code i) -> four fp16 values, exactly: .x holds
+// codes 0, 1 and .y codes 2, 3 (low half first).  A NaN code gives a NaN.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t codes) {
+  uint32_t lo, hi;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
+  return make_uint2(lo, hi);
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` in a 16-row x D e4m3 tile that
+// TMA wrote with the D-byte swizzle (128 B: chunk ^= r % 8; 64 B: chunk ^=
+// (r / 2) % 4, i.e. address bits 4-5 XOR bits 7-8).
+template <int D>
+__device__ __forceinline__ uint32_t swz8(int r, int c) {
+  if constexpr (D == 128) return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+  else return static_cast<uint32_t>(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Operand-type switch of the mma.sync kernels: bf16 (bf16 caches) or fp16
+// (FP8 caches).
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (F16) mma_f16_16816(d, a0, a1, a2, a3, b0, b1);
+  else mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) return pack_f16(lo, hi);
+  else return pack_bf16(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float lo2(uint32_t x) {
+  if constexpr (F16) return f16_lo(x);
+  else return bf16_lo(x);
+}
+template <bool F16>
+__device__ __forceinline__ float hi2(uint32_t x) {
+  if constexpr (F16) return f16_hi(x);
+  else return bf16_hi(x);
+}
+
+// bf16 query values -> fp16 for the FP8 kernels.  A row whose largest
+// magnitude exceeds 2^14 is first scaled by a power of two 2^-e (exact) so
+// that it stays inside the fp16 range; the caller multiplies that row's
+// scores by 2^e.  Returns e (0 for rows in range, or non-finite ones).
+__device__ __forceinline__ int f16_row_exponent(float amax) {
+  if (!(amax > 16384.f) || !(amax <= 3.402823466e38f)) return 0;
+  return ((__float_as_int(amax) >> 23) & 0xFF) - 127 + 1 - 14;  // amax * 2^-e < 2^14
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float mul) {
+  return pack_f16(bf16_lo(w) * mul, bf16_hi(w) * mul);
+}
 
 // Byte offset of element (row, d) inside one 16-row x head_size bf16 tile that
 // TMA wrote as head_size/64 boxes of 16 rows x 128 B with the 128-byte

@@ -37,30 +37,40 @@ namespace {
 
 constexpr int kDecodeWarps = 4;
 
-template <int D>
+template <int D, bool FP8>
 struct DecodeTile {
-  static constexpr int kHalves = D / 64;           // 64-column TMA boxes per row
-  static constexpr int kTileBytes = D * 2 * kBlock;  // one 16-key block of K (or V)
-  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kHalves = D / 64;             // 64-column TMA boxes per row
+  static constexpr int kTileBytes = D * 2 * kBlock;  // one 16-key block of K (or V), bf16
+  // what TMA lands per block: bf16 tiles, or e4m3 codes (D bytes per row)
+  static constexpr int kLoadBytes = FP8 ? D * kBlock : kTileBytes;
+  static constexpr int kStageBytes = 2 * kLoadBytes;
 };
 
-template <int D, int NS>
+template <int D, int NS, bool FP8>
 constexpr int decode_smem_bytes() {
-  return 1024 /* alignment slack */ + kDecodeWarps * NS * DecodeTile<D>::kStageBytes +
+  using T = DecodeTile<D, FP8>;
+  return 1024 /* alignment slack */ + kDecodeWarps * NS * T::kStageBytes +
          kDecodeWarps * NS * 8 /* mbarriers */ + 2 * kDecodeWarps * 8 * 4 /* merge factors */;
 }
 
-template <int D, int NS>
+
+template <int D, int NS, bool FP8>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     pkv_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using T = DecodeTile<D>;
+  using T = DecodeTile<D, FP8>;
   constexpr int NW = kDecodeWarps;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NS * T::kStageBytes);
   float* merge_f = reinterpret_cast<float*>(bars + NW * NS);  // [NW][8] factors, [8] lse
+  // Merge area of warp w ([8 heads][D] + m[8] + l[8] floats): the start of its
+  // stage ring, free once its loads are consumed.
+  static_assert(NS * T::kStageBytes >= (8 * D + 16) * 4, "merge area exceeds the ring");
+  auto merge_area = [&](int w) {
+    return reinterpret_cast<float*>(smem + w * NS * T::kStageBytes);
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -138,11 +148,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       const uint32_t bar = bar0 + 8 * st;
       if (ok) {
         mbar_arrive_expect_tx(bar, T::kStageBytes);
+        if constexpr (FP8) {  // one box of 16 rows x D codes per block
+          tma_load_3d(dst, &kmap, bar, 0, kvh, bid * kBlock, policy);
+          tma_load_3d(dst + T::kLoadBytes, &vmap, bar, 0, kvh, bid * kBlock, policy);
+        } else {
 #pragma unroll
-        for (int h = 0; h < T::kHalves; ++h) {
-          tma_load_3d(dst + h * 2048, &kmap, bar, h * 64, kvh, bid * kBlock, policy);
-          tma_load_3d(dst + T::kTileBytes + h * 2048, &vmap, bar, h * 64, kvh, bid * kBlock,
-                      policy);
+          for (int h = 0; h < T::kHalves; ++h) {
+            tma_load_3d(dst + h * 2048, &kmap, bar, h * 64, kvh, bid * kBlock, policy);
+            tma_load_3d(dst + T::kTileBytes + h * 2048, &vmap, bar, h * 64, kvh, bid * kBlock,
+                        policy);
+          }
         }
       } else {
         mbar_arrive(bar);  // nothing to load: complete the phase empty
@@ -156,6 +171,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   // Q^T as the B operand: lane holds Q[g = lane/4][kk*16 + 2*(lane%4) + {0,1}]
   // (qb[kk][0]) and the same +8 (qb[kk][1]); heads past the group are zero.
+  // FP8: the contraction runs over a permutation of d instead (any order
+  // gives the same dot products), chosen so that a lane's K codes are
+  // contiguous: step kk, k-slots {2t, 2t+1, 2t+8, 2t+9} (t = lane % 4) are
+  // d = (D/4) t + 4 kk + {0, 1, 2, 3}.
   uint32_t qb[D / 16][2];
   {
     const int g = gsub * 8 + (lane >> 2);
@@ -165,9 +184,41 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         (static_cast<int64_t>(q0) * Hq + kvh * G + (gv ? g : 0)) * D);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      qb[kk][0] = gv ? __ldg(qrow + kk * 8 + (lane & 3)) : 0u;
-      qb[kk][1] = gv ? __ldg(qrow + kk * 8 + 4 + (lane & 3)) : 0u;
+      if constexpr (FP8) {
+        qb[kk][0] = gv ? __ldg(qrow + (D / 8) * (lane & 3) + 2 * kk) : 0u;
+        qb[kk][1] = gv ? __ldg(qrow + (D / 8) * (lane & 3) + 2 * kk + 1) : 0u;
+      } else {
+        qb[kk][0] = gv ? __ldg(qrow + kk * 8 + (lane & 3)) : 0u;
+        qb[kk][1] = gv ? __ldg(qrow + kk * 8 + 4 + (lane & 3)) : 0u;
+      }
     }
+  }
+
+  // FP8: the MMAs run on fp16 operands.  K = code * k_descale folds into the
+  // score scale, V = code * v_descale into the output; Q goes to fp16, a head
+  // whose values exceed 2^14 scaled down by 2^e first and its scores up by 2^e.
+  float scale_log2 = a.scale_log2, out_scale = 1.f;
+  float col_scale[2] = {scale_log2, scale_log2};  // score scale of head columns c0, c0 + 1
+  if constexpr (FP8) {
+    scale_log2 *= __ldg(a.k_descale + static_cast<int64_t>(s) * a.num_kv_heads + kvh);
+    out_scale = __ldg(a.v_descale + static_cast<int64_t>(s) * a.num_kv_heads + kvh);
+    float amax = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(qb[kk][j])), fabsf(bf16_hi(qb[kk][j]))));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the 4 lanes of head lane/4
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int e = f16_row_exponent(amax);
+    const float down = pow2f(-e);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) qb[kk][j] = bf16x2_to_f16x2(qb[kk][j], down);
+    const int c0 = 2 * (lane & 3);
+    col_scale[0] = scale_log2 * pow2f(__shfl_sync(0xffffffffu, e, 4 * c0));
+    col_scale[1] = scale_log2 * pow2f(__shfl_sync(0xffffffffu, e, 4 * c0 + 4));
   }
 
   float o[D / 16][4];
@@ -186,8 +237,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   for (int i = 0; i < nb_w; ++i) {
     const int st = i % NS;
-    const uint32_t kbuf = wbase_u + st * T::kStageBytes;
-    const uint32_t vbuf = kbuf + T::kTileBytes;
+    uint32_t kbuf = wbase_u + st * T::kStageBytes;
+    uint32_t vbuf = kbuf + T::kTileBytes;
     const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
     if (!mbar_wait(bar0 + 8 * st, (i / NS) & 1)) {
       timed_out = true;
@@ -197,21 +248,41 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       const int p0 = (b_begin + warp + NW * i) * kBlock;  // first key of the block
       // ---- S^T = K . Q^T  (16 keys x 8 heads)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (FP8) {
+        // K fragments straight from the codes: rows r0 and r0 + 8, bytes
+        // [(D/4) t, (D/4) t + D/4) (the permuted d above), widened to fp16.
+        const uint8_t* kt = wbase + st * T::kStageBytes;
+        constexpr int KC = D / 64;  // 16-byte chunks per lane and row
+        uint4 kw[2][KC];
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(kbuf + swz_offset(k_row, kk * 16 + k_dsub), a0, a1, a2, a3);
-        mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < KC; ++c)
+            kw[h][c] = *reinterpret_cast<const uint4*>(kt + swz8<D>(r0 + 8 * h, KC * (lane & 3) + c));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk / 4]);
+          const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk / 4]);
+          const uint2 x = e4m3x4_to_f16x4(w0[kk % 4]), y = e4m3x4_to_f16x4(w1[kk % 4]);
+          mma_16816<true>(sc, x.x, y.x, x.y, y.y, qb[kk][0], qb[kk][1]);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kbuf + swz_offset(k_row, kk * 16 + k_dsub), a0, a1, a2, a3);
+          mma_16816<false>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
       }
       // ---- mask keys past the context (they may hold stale NaN) and before
       //      the window
       const bool v0 = p0 + r0 < L && p0 + r0 >= kfirst;
       const bool v1 = p0 + r0 + 8 < L && p0 + r0 + 8 >= kfirst;
       float x[4];
-      x[0] = v0 ? sc[0] * a.scale_log2 : -INFINITY;
-      x[1] = v0 ? sc[1] * a.scale_log2 : -INFINITY;
-      x[2] = v1 ? sc[2] * a.scale_log2 : -INFINITY;
-      x[3] = v1 ? sc[3] * a.scale_log2 : -INFINITY;
+      x[0] = v0 ? sc[0] * col_scale[0] : -INFINITY;
+      x[1] = v0 ? sc[1] * col_scale[1] : -INFINITY;
+      x[2] = v1 ? sc[2] * col_scale[0] : -INFINITY;
+      x[3] = v1 ? sc[3] * col_scale[1] : -INFINITY;
       // ---- online softmax per head column c (keys spread over lane/4)
       float alpha[2];
       uint32_t pk0, pk1;
@@ -229,10 +300,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         alpha[1] = exp2f(m[1] - mu1);
         m[0] = mn0;
         m[1] = mn1;
-        pk0 = pack_bf16(exp2f(x[0] - mu0), exp2f(x[1] - mu1));  // key r0, heads c0,c1
-        pk1 = pack_bf16(exp2f(x[2] - mu0), exp2f(x[3] - mu1));  // key r0+8
-        l[0] = l[0] * alpha[0] + bf16_lo(pk0) + bf16_lo(pk1);
-        l[1] = l[1] * alpha[1] + bf16_hi(pk0) + bf16_hi(pk1);
+        pk0 = pack2<FP8>(exp2f(x[0] - mu0), exp2f(x[1] - mu1));  // key r0, heads c0,c1
+        pk1 = pack2<FP8>(exp2f(x[2] - mu0), exp2f(x[3] - mu1));  // key r0+8
+        l[0] = l[0] * alpha[0] + lo2<FP8>(pk0) + lo2<FP8>(pk1);
+        l[1] = l[1] * alpha[1] + hi2<FP8>(pk0) + hi2<FP8>(pk1);
       }
 #pragma unroll
       for (int dt = 0; dt < D / 16; ++dt) {
@@ -244,7 +315,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       const uint32_t pb0 = movmatrix_trans(pk0);  // P^T rows = heads, keys 0..7
       const uint32_t pb1 = movmatrix_trans(pk1);  // keys 8..15
       // ---- the sequence's last, partial block: zero V rows past the context
-      if (p0 + kBlock > L) {
+      //      (FP8: zeroed in registers below)
+      if (!FP8 && p0 + kBlock > L) {
         const int nvalid = L - p0;
         uint8_t* vrow = wbase + st * T::kStageBytes + T::kTileBytes;
         for (int e = lane; e < (kBlock - nvalid) * T::kHalves * 8; e += 32) {
@@ -257,11 +329,46 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         __syncwarp();
       }
       // ---- O^T += V^T . P^T
+      if constexpr (FP8) {
+        // V^T fragments from the codes of key rows 2t, 2t+1, 2t+8, 2t+9: the
+        // output rows of step dt are d = (D/8) r0 + 2 dt + {0, 1} (a
+        // permutation of d undone in the merge), so a lane reads bytes
+        // [(D/8) r0, (D/8) r0 + D/8) of each of its four rows.
+        const uint8_t* vt = wbase + st * T::kStageBytes + T::kLoadBytes;
+        constexpr int VW = D / 32;  // 32-bit words per lane and row
+        uint32_t vw[4][VW];
+        const int t = lane & 3;
 #pragma unroll
-      for (int dt = 0; dt < D / 16; ++dt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_trans(vbuf + swz_offset(v_row, dt * 16 + v_dsub), a0, a1, a2, a3);
-        mma_bf16_16816(o[dt], a0, a1, a2, a3, pb0, pb1);
+        for (int q = 0; q < 4; ++q) {
+          const int row = 2 * t + (q & 1) + 8 * (q >> 1);
+          if constexpr (D == 128) {
+            const uint4 u = *reinterpret_cast<const uint4*>(vt + swz8<D>(row, r0));
+            vw[q][0] = u.x; vw[q][1] = u.y; vw[q][2] = u.z; vw[q][3] = u.w;
+          } else {
+            const uint2 u = *reinterpret_cast<const uint2*>(vt + swz8<D>(row, r0 >> 1) +
+                                                            8 * (r0 & 1));
+            vw[q][0] = u.x; vw[q][1] = u.y;
+          }
+          if (p0 + row >= L) {  // past the context: stale codes, NaN included
+#pragma unroll
+            for (int w = 0; w < VW; ++w) vw[q][w] = 0u;
+          }
+        }
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt) {
+          // bytes 2dt, 2dt+1 of rows (2t, 2t+1) interleaved: (k0,d0) (k1,d0) (k0,d1) (k1,d1)
+          const uint32_t sel = (dt & 1) ? 0x7362u : 0x5140u;
+          const uint2 lo = e4m3x4_to_f16x4(prmt(vw[0][dt / 2], vw[1][dt / 2], sel));
+          const uint2 hi = e4m3x4_to_f16x4(prmt(vw[2][dt / 2], vw[3][dt / 2], sel));
+          mma_16816<true>(o[dt], lo.x, lo.y, hi.x, hi.y, pb0, pb1);
+        }
+      } else {
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(vbuf + swz_offset(v_row, dt * 16 + v_dsub), a0, a1, a2, a3);
+          mma_16816<false>(o[dt], a0, a1, a2, a3, pb0, pb1);
+        }
       }
     }
     __syncwarp();
@@ -290,16 +397,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
   }
 
-  // ---- merge the warps through shared memory (each warp reuses its stage 0)
-  float* wo = reinterpret_cast<float*>(wbase);  // [8 heads][D] then m[8], l[8]
+  // ---- merge the warps through shared memory
+  float* wo = merge_area(warp);  // [8 heads][D] then m[8], l[8]
 #pragma unroll
   for (int dt = 0; dt < D / 16; ++dt) {
-    const int d = dt * 16 + r0;
+    // output rows r0 and r0 + 8 of step dt hold d and d + dd
+    const int d = FP8 ? (D / 8) * r0 + 2 * dt : dt * 16 + r0;
+    constexpr int dd = FP8 ? 1 : 8;
     const int c = 2 * (lane & 3);
     wo[c * D + d] = o[dt][0];
     wo[(c + 1) * D + d] = o[dt][1];
-    wo[c * D + d + 8] = o[dt][2];
-    wo[(c + 1) * D + d + 8] = o[dt][3];
+    wo[c * D + d + dd] = o[dt][2];
+    wo[(c + 1) * D + d + dd] = o[dt][3];
   }
   if (lane < 4) {
     wo[8 * D + 2 * lane] = m[0];
@@ -311,16 +420,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   if (threadIdx.x < 8) {
     const int c = threadIdx.x;
     float M = -INFINITY;
-    for (int w = 0; w < NW; ++w)
-      M = fmaxf(M, reinterpret_cast<float*>(smem + w * NS * T::kStageBytes)[8 * D + c]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, merge_area(w)[8 * D + c]);
     float den = 0.f;
     float f[NW];
     for (int w = 0; w < NW; ++w) {
-      const float* ww = reinterpret_cast<float*>(smem + w * NS * T::kStageBytes);
+      const float* ww = merge_area(w);
       f[w] = (M == -INFINITY) ? 0.f : exp2f(ww[8 * D + c] - M);
       den += f[w] * ww[8 * D + 8 + c];
     }
-    for (int w = 0; w < NW; ++w) merge_f[w * 8 + c] = den > 0.f ? f[w] / den : 0.f;
+    for (int w = 0; w < NW; ++w) merge_f[w * 8 + c] = den > 0.f ? f[w] * out_scale / den : 0.f;
     merge_f[NW * 8 + c] = den > 0.f ? M + log2f(den) : -INFINITY;
   }
   __syncthreads();
@@ -333,8 +441,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     if (g >= G) continue;
     float r = 0.f;
 #pragma unroll
-    for (int w = 0; w < NW; ++w)
-      r += merge_f[w * 8 + c] * reinterpret_cast<float*>(smem + w * NS * T::kStageBytes)[c * D + d];
+    for (int w = 0; w < NW; ++w) r += merge_f[w * 8 + c] * merge_area(w)[c * D + d];
     const int hq = kvh * G + g;
     if (direct) {
       out[(static_cast<int64_t>(q0) * Hq + hq) * D + d] = __float2bfloat16(r);
@@ -424,11 +531,11 @@ __global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs 
         __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
 }
 
-template <int D, int NS>
+template <int D, int NS, bool FP8>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
                             const DecodeArgs& a, cudaStream_t stream) {
-  constexpr int smem = decode_smem_bytes<D, NS>();
-  auto kfn = pkv_decode_bf16_kernel<D, NS>;
+  constexpr int smem = decode_smem_bytes<D, NS, FP8>();
+  auto kfn = pkv_decode_bf16_kernel<D, NS, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int ngsub = (a.group + 7) / 8;
@@ -441,11 +548,18 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
 
 // Stages per warp: 3 x 8 KB (head_size 128) keeps 2 CTAs (8 warps, up to 16
 // blocks = 128 KB of K/V) in flight per SM.
+// FP8 stages are half the size: 4-deep rings still leave room for three CTAs
+// per SM.
 cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               const DecodeArgs& a, int head_size, cudaStream_t stream) {
+                               const DecodeArgs& a, int head_size, bool fp8,
+                               cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
-  if (head_size == 128) return launch_decode_t<128, 3>(kmap, vmap, a, stream);
-  return launch_decode_t<64, 4>(kmap, vmap, a, stream);
+  if (fp8) {
+    if (head_size == 128) return launch_decode_t<128, 4, true>(kmap, vmap, a, stream);
+    return launch_decode_t<64, 6, true>(kmap, vmap, a, stream);
+  }
+  if (head_size == 128) return launch_decode_t<128, 3, false>(kmap, vmap, a, stream);
+  return launch_decode_t<64, 4, false>(kmap, vmap, a, stream);
 }
 
 cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream) {

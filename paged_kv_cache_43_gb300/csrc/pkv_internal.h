@@ -23,6 +23,10 @@ struct WriteArgs {
   int64_t num_slots;    // num_blocks * block_size
   int32_t num_tokens;
   int32_t row_vecs;     // 16-byte vectors per token row (num_kv_heads*head_size*bytes/16)
+  // FP8 cache: per-kv-head quantisation scales (null otherwise)
+  const float* k_scale;
+  const float* v_scale;
+  int32_t head_size;
 };
 
 // Split-K decode over sequences [0, num_seqs) (each with one query row).
@@ -46,6 +50,8 @@ struct DecodeArgs {
   int32_t num_tokens;            // rows of q/out: query_start_loc must stay inside
   int32_t max_context_len;       // bound the split buffer was sized for
   int32_t window;                // sliding window (keys per query), 0 = none
+  const float* k_descale;        // FP8 cache: [num_seqs_total, Hkv] (null otherwise)
+  const float* v_descale;
   float scale_log2;              // scale * log2(e)
 };
 
@@ -68,6 +74,8 @@ struct PrefillArgs {
   int32_t num_tokens;
   int32_t max_query_len;
   int32_t window;                // sliding window (keys per query), 0 = none
+  const float* k_descale;        // FP8 cache: [num_seqs_total, Hkv] (null otherwise)
+  const float* v_descale;
   float scale_log2;
 };
 
@@ -93,11 +101,15 @@ struct F32Args {
 };
 
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream, int num_sms);
+cudaError_t launch_write_fp8(const WriteArgs& a, cudaStream_t stream, int num_sms);
+// fp8 = true: the caches hold e4m3 codes (the maps are uint8, unswizzled).
 cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               const DecodeArgs& a, int head_size, cudaStream_t stream);
+                               const DecodeArgs& a, int head_size, bool fp8,
+                               cudaStream_t stream);
 cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                const PrefillArgs& a, int head_size, cudaStream_t stream);
+                                const PrefillArgs& a, int head_size, bool fp8,
+                                cudaStream_t stream);
 cudaError_t launch_attention_f32(const F32Args& a, cudaStream_t stream);
 
 // tcgen05 prefill: query tiles of 128 rows = (128 / group) tokens x group heads,

@@ -16,15 +16,18 @@ import torch
 _lock = threading.Lock()
 _lib = None
 
-PKV_F32, PKV_BF16 = 0, 1
+PKV_F32, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
+# FP8 caches hold e4m3 codes; either dtype may carry them.
+FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn)
 ERR_SLOT = 1 << 0
 ERR_BLOCK_ID = 1 << 1
 ERR_CONTEXT_LEN = 1 << 2
 ERR_QUERY_LEN = 1 << 3
 ERR_DECODE_QLEN = 1 << 4
 ERR_TIMEOUT = 1 << 5
-EXPORTED = ("pkv_write", "pkv_attention_workspace_size", "pkv_attention",
-            "pkv_attention_static_scratch", "pkv_get_error", "pkv_status_string")
+EXPORTED = ("pkv_write", "pkv_write_fp8", "pkv_attention_workspace_size", "pkv_attention",
+            "pkv_attention_fp8", "pkv_attention_static_scratch", "pkv_get_error",
+            "pkv_status_string")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -71,6 +74,13 @@ def load(path: str | None = None):
         lib.pkv_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                       ctypes.POINTER(CacheDesc), ctypes.POINTER(AttnMeta),
                                       vp, ctypes.c_size_t, vp]
+        lib.pkv_write_fp8.restype = ctypes.c_int
+        lib.pkv_write_fp8.argtypes = [vp, vp, i64p, i32, vp, vp, vp, vp,
+                                      ctypes.POINTER(CacheDesc), vp]
+        lib.pkv_attention_fp8.restype = ctypes.c_int
+        lib.pkv_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                          ctypes.POINTER(CacheDesc), ctypes.POINTER(AttnMeta),
+                                          vp, ctypes.c_size_t, vp]
         lib.pkv_attention_static_scratch.restype = ctypes.c_int
         lib.pkv_attention_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                                      ctypes.POINTER(CacheDesc),
@@ -93,6 +103,8 @@ def _dtype_code(t: torch.Tensor) -> int:
         return PKV_BF16
     if t.dtype == torch.float32:
         return PKV_F32
+    if t.dtype in FP8_DTYPES:
+        return PKV_FP8_E4M3
     raise PkvError(f"unsupported dtype {t.dtype}")
 
 
@@ -130,6 +142,31 @@ def write(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
     _check(lib.pkv_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
                          k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
                          _stream(stream)))
+
+
+def write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None) -> None:
+    """pkv_write_fp8: quantise bf16 k/v [T, Hkv, D] with the per-kv-head
+    scales (fp32 [Hkv]) into the e4m3 caches at slot_mapping[T]."""
+    lib = load()
+    for t, n in ((k, "k"), (v, "v")):
+        _require(t, n, dtype=torch.bfloat16)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n)
+        if t.dtype not in FP8_DTYPES:
+            raise PkvError(f"{n} must hold e4m3 codes (uint8 or float8_e4m3fn)")
+    hkv = k_cache.shape[2]
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _require(t, n, dtype=torch.float32, ndim=1)
+        if t.shape[0] != hkv:
+            raise PkvError(f"{n} must have num_kv_heads entries")
+    _require(slot_mapping, "slot_mapping", dtype=torch.int64, ndim=1)
+    T = slot_mapping.shape[0]
+    if k.shape[0] < T or v.shape[0] < T:
+        raise PkvError("k/v have fewer rows than slot_mapping")
+    desc = cache_desc(k_cache)
+    _check(lib.pkv_write_fp8(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                             k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+                             v_scale.data_ptr(), ctypes.byref(desc), _stream(stream)))
 
 
 def attn_meta(q, block_tables, context_lens, *, max_query_len, max_context_len,
@@ -174,6 +211,44 @@ def attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start_
                              context_lens.data_ptr(), query_start_loc.data_ptr(),
                              float(scale), ctypes.byref(desc), ctypes.byref(meta),
                              ws_ptr, ws_bytes, _stream(stream)))
+
+
+def attention_fp8(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
+                  k_descale, v_descale, *, max_query_len, max_context_len, num_decode_seqs=-1,
+                  kv_split_tokens=0, sliding_window=0, workspace=None, stream=None) -> None:
+    """pkv_attention_fp8 into ``out`` [T, Hq, D] (bf16) over e4m3 caches;
+    ``k_descale``/``v_descale`` fp32 [num_seqs, Hkv]."""
+    lib = load()
+    for t, n in ((out, "out"), (q, "q")):
+        _require(t, n, dtype=torch.bfloat16)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n)
+        if t.dtype not in FP8_DTYPES:
+            raise PkvError(f"{n} must hold e4m3 codes (uint8 or float8_e4m3fn)")
+    _require(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _require(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    _require(query_start_loc, "query_start_loc", dtype=torch.int32, ndim=1)
+    for t, n in ((k_descale, "k_descale"), (v_descale, "v_descale")):
+        _require(t, n, dtype=torch.float32, ndim=2)
+        if tuple(t.shape) != (context_lens.shape[0], k_cache.shape[2]):
+            raise PkvError(f"{n} must be [num_seqs, num_kv_heads]")
+    if out.shape != q.shape:
+        raise PkvError("out and q must have the same shape")
+    meta = attn_meta(q, block_tables, context_lens, max_query_len=max_query_len,
+                     max_context_len=max_context_len, num_decode_seqs=num_decode_seqs,
+                     kv_split_tokens=kv_split_tokens, sliding_window=sliding_window)
+    desc = cache_desc(k_cache)
+    need = workspace_size(k_cache, meta)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.pkv_attention_fp8(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(),
+                                 v_cache.data_ptr(), block_tables.data_ptr(),
+                                 context_lens.data_ptr(), query_start_loc.data_ptr(),
+                                 float(scale), k_descale.data_ptr(), v_descale.data_ptr(),
+                                 ctypes.byref(desc), ctypes.byref(meta), ws_ptr, ws_bytes,
+                                 _stream(stream)))
 
 
 def attention_static_scratch(out, q, k_cache, v_cache, block_tables, context_lens,

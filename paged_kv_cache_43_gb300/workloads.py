@@ -249,6 +249,28 @@ def workload(n: int, *, small: bool = False, device="cpu", poison=True,
     return make_workload(q_lens, ctx, dtype=torch.bfloat16, **kw)
 
 
+def history_slots(wl: Workload) -> np.ndarray:
+    """Sorted unique cache slots of the keys written before this step
+    (positions 0 .. L - q_s - 1 of every sequence), for filling a cache of
+    another dtype from the same history."""
+    bt = wl.block_tables.cpu().numpy()
+    parts = []
+    for s in range(wl.num_seqs):
+        pos = np.arange(int(wl.ctx_lens[s]) - int(wl.q_lens[s]))
+        parts.append(bt[s, pos // BLOCK_SIZE].astype(np.int64) * BLOCK_SIZE + pos % BLOCK_SIZE)
+    return np.unique(np.concatenate(parts)) if parts else np.zeros(0, np.int64)
+
+
+def fp8_scales(num_kv_heads: int, seed: int, lo: float = 0.008, hi: float = 0.03) -> np.ndarray:
+    """Per-kv-head fp32 quantisation scales for an e4m3 cache, drawn uniformly
+    in [lo, hi] (N(0, 1) data then spans roughly 1/8 .. 1/2 of the e4m3 range)."""
+    rng = np.random.default_rng(seed)
+    return rng.uniform(lo, hi, size=num_kv_heads).astype(np.float32)
+
+
+E4M3_NAN_CODE = 0x7F   # filler for slots with no live key (an e4m3 NaN)
+
+
 def cache_bytes_per_block(num_kv_heads: int, head_size: int, dtype: torch.dtype) -> int:
     """Bytes the two caches allocate per block, measured from real tensors."""
     k = torch.empty((1, BLOCK_SIZE, num_kv_heads, head_size), dtype=dtype)
