@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   // Merge area of warp w ([8 heads][D] + m[8] + l[8] floats): the start of its
   // stage ring, free once its loads are consumed.
   static_assert(NS * T::kStageBytes >= (8 * D + 16) * 4, "merge area exceeds the ring");
+  static_assert(T::kHalves >= 1, "head_size 64 or 128");
   auto merge_area = [&](int w) {
     return reinterpret_cast<float*>(smem + w * NS * T::kStageBytes);
   };
@@ -235,109 +236,86 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int r0 = lane >> 2;                                // score rows (keys) r0, r0 + 8
   bool timed_out = false;
 
+  // One block's online-softmax step: scores sc (S^T: keys r0, r0 + 8 x head
+  // columns c0, c0 + 1) of the block starting at key p0 -> probabilities as
+  // the P^T operand (pb0: keys 0..7, pb1: keys 8..15); updates m, l and O.
+  // The reference max m of a column moves only when a score exceeds it by more
+  // than 8 (log2 units): the probabilities then stay below 2^8 (as exact in
+  // 16 bits as any, summed in fp32), and the common case costs one warp vote
+  // instead of a shuffle reduction and a rescale of O.  The exponent reference
+  // cancels in O / l, so the result is the same softmax.
+  auto softmax_step = [&](const float (&sc)[4], int p0, uint32_t& pb0, uint32_t& pb1) {
+    // mask keys past the context (they may hold stale NaN) and before the window
+    const bool v0 = p0 + r0 < L && p0 + r0 >= kfirst;
+    const bool v1 = p0 + r0 + 8 < L && p0 + r0 + 8 >= kfirst;
+    float x[4];
+    x[0] = v0 ? sc[0] * col_scale[0] : -INFINITY;
+    x[1] = v0 ? sc[1] * col_scale[1] : -INFINITY;
+    x[2] = v1 ? sc[2] * col_scale[0] : -INFINITY;
+    x[3] = v1 ? sc[3] * col_scale[1] : -INFINITY;
+    const float lim0 = m[0] + 8.f, lim1 = m[1] + 8.f;
+    const bool grow = x[0] > lim0 || x[1] > lim1 || x[2] > lim0 || x[3] > lim1;
+    if (__any_sync(0xffffffffu, grow)) {
+      // new reference: the column max over the block's keys (lanes of equal t)
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+      const float alpha0 = mn0 == -INFINITY ? 1.f : exp2f(m[0] - mn0);
+      const float alpha1 = mn1 == -INFINITY ? 1.f : exp2f(m[1] - mn1);
+      m[0] = mn0;
+      m[1] = mn1;
+      l[0] *= alpha0;
+      l[1] *= alpha1;
+#pragma unroll
+      for (int dt = 0; dt < D / 16; ++dt) {
+        o[dt][0] *= alpha0;
+        o[dt][1] *= alpha1;
+        o[dt][2] *= alpha0;
+        o[dt][3] *= alpha1;
+      }
+    }
+    const float mu0 = m[0] == -INFINITY ? 0.f : m[0];  // all keys so far masked
+    const float mu1 = m[1] == -INFINITY ? 0.f : m[1];
+    const uint32_t pk0 = pack2<FP8>(exp2f(x[0] - mu0), exp2f(x[1] - mu1));  // key r0
+    const uint32_t pk1 = pack2<FP8>(exp2f(x[2] - mu0), exp2f(x[3] - mu1));  // key r0 + 8
+    l[0] += lo2<FP8>(pk0) + lo2<FP8>(pk1);
+    l[1] += hi2<FP8>(pk0) + hi2<FP8>(pk1);
+    pb0 = movmatrix_trans(pk0);  // P^T rows = heads
+    pb1 = movmatrix_trans(pk1);
+  };
+
   for (int i = 0; i < nb_w; ++i) {
     const int st = i % NS;
-    uint32_t kbuf = wbase_u + st * T::kStageBytes;
-    uint32_t vbuf = kbuf + T::kTileBytes;
     const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
     if (!mbar_wait(bar0 + 8 * st, (i / NS) & 1)) {
       timed_out = true;
       break;
     }
-    if (ok) {
-      const int p0 = (b_begin + warp + NW * i) * kBlock;  // first key of the block
-      // ---- S^T = K . Q^T  (16 keys x 8 heads)
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (FP8) {
-        // K fragments straight from the codes: rows r0 and r0 + 8, bytes
-        // [(D/4) t, (D/4) t + D/4) (the permuted d above), widened to fp16.
+    const int p0 = (b_begin + warp + NW * i) * kBlock;  // first key of the block
+    if constexpr (FP8) {
+      // The whole block goes to registers first, so that its stage is
+      // refilled before the block is computed (all NS loads stay in flight).
+      // K: rows r0 and r0 + 8, bytes [(D/4) t, (D/4) t + D/4) (the permuted d
+      // above).  V: rows 2t, 2t+1, 2t+8, 2t+9, bytes [(D/8) r0, (D/8) r0 +
+      // D/8): the PV output rows of step dt are d = (D/8) r0 + 2 dt + {0, 1},
+      // a permutation of d undone in the merge.
+      constexpr int KC = D / 64;  // 16-byte K chunks per lane and row
+      constexpr int VW = D / 32;  // 32-bit V words per lane and row
+      const int t = lane & 3;
+      uint4 kw[2][KC];
+      uint32_t vw[4][VW];
+      if (ok) {
         const uint8_t* kt = wbase + st * T::kStageBytes;
-        constexpr int KC = D / 64;  // 16-byte chunks per lane and row
-        uint4 kw[2][KC];
+        const uint8_t* vt = kt + T::kLoadBytes;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int c = 0; c < KC; ++c)
-            kw[h][c] = *reinterpret_cast<const uint4*>(kt + swz8<D>(r0 + 8 * h, KC * (lane & 3) + c));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk / 4]);
-          const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk / 4]);
-          const uint2 x = e4m3x4_to_f16x4(w0[kk % 4]), y = e4m3x4_to_f16x4(w1[kk % 4]);
-          mma_16816<true>(sc, x.x, y.x, x.y, y.y, qb[kk][0], qb[kk][1]);
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(kbuf + swz_offset(k_row, kk * 16 + k_dsub), a0, a1, a2, a3);
-          mma_16816<false>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-        }
-      }
-      // ---- mask keys past the context (they may hold stale NaN) and before
-      //      the window
-      const bool v0 = p0 + r0 < L && p0 + r0 >= kfirst;
-      const bool v1 = p0 + r0 + 8 < L && p0 + r0 + 8 >= kfirst;
-      float x[4];
-      x[0] = v0 ? sc[0] * col_scale[0] : -INFINITY;
-      x[1] = v0 ? sc[1] * col_scale[1] : -INFINITY;
-      x[2] = v1 ? sc[2] * col_scale[0] : -INFINITY;
-      x[3] = v1 ? sc[3] * col_scale[1] : -INFINITY;
-      // ---- online softmax per head column c (keys spread over lane/4)
-      float alpha[2];
-      uint32_t pk0, pk1;
-      {
-        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        alpha[0] = exp2f(m[0] - mu0);
-        alpha[1] = exp2f(m[1] - mu1);
-        m[0] = mn0;
-        m[1] = mn1;
-        pk0 = pack2<FP8>(exp2f(x[0] - mu0), exp2f(x[1] - mu1));  // key r0, heads c0,c1
-        pk1 = pack2<FP8>(exp2f(x[2] - mu0), exp2f(x[3] - mu1));  // key r0+8
-        l[0] = l[0] * alpha[0] + lo2<FP8>(pk0) + lo2<FP8>(pk1);
-        l[1] = l[1] * alpha[1] + hi2<FP8>(pk0) + hi2<FP8>(pk1);
-      }
-#pragma unroll
-      for (int dt = 0; dt < D / 16; ++dt) {
-        o[dt][0] *= alpha[0];
-        o[dt][1] *= alpha[1];
-        o[dt][2] *= alpha[0];
-        o[dt][3] *= alpha[1];
-      }
-      const uint32_t pb0 = movmatrix_trans(pk0);  // P^T rows = heads, keys 0..7
-      const uint32_t pb1 = movmatrix_trans(pk1);  // keys 8..15
-      // ---- the sequence's last, partial block: zero V rows past the context
-      //      (FP8: zeroed in registers below)
-      if (!FP8 && p0 + kBlock > L) {
-        const int nvalid = L - p0;
-        uint8_t* vrow = wbase + st * T::kStageBytes + T::kTileBytes;
-        for (int e = lane; e < (kBlock - nvalid) * T::kHalves * 8; e += 32) {
-          const int r = nvalid + e / (T::kHalves * 8);
-          const int rem = e % (T::kHalves * 8);
-          *reinterpret_cast<uint4*>(vrow + (rem >> 3) * 2048 + r * 128 + (rem & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async();  // before any later TMA write to this stage
-        __syncwarp();
-      }
-      // ---- O^T += V^T . P^T
-      if constexpr (FP8) {
-        // V^T fragments from the codes of key rows 2t, 2t+1, 2t+8, 2t+9: the
-        // output rows of step dt are d = (D/8) r0 + 2 dt + {0, 1} (a
-        // permutation of d undone in the merge), so a lane reads bytes
-        // [(D/8) r0, (D/8) r0 + D/8) of each of its four rows.
-        const uint8_t* vt = wbase + st * T::kStageBytes + T::kLoadBytes;
-        constexpr int VW = D / 32;  // 32-bit words per lane and row
-        uint32_t vw[4][VW];
-        const int t = lane & 3;
+            kw[h][c] = *reinterpret_cast<const uint4*>(kt + swz8<D>(r0 + 8 * h, KC * t + c));
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int row = 2 * t + (q & 1) + 8 * (q >> 1);
@@ -354,6 +332,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             for (int w = 0; w < VW; ++w) vw[q][w] = 0u;
           }
         }
+      }
+      __syncwarp();
+      if (i + NS < nb_w) {
+        if (lane == 0) fence_proxy_async();
+        issue(i + NS);
+        ++issued;
+      }
+      if (ok) {
+        // ---- S^T = K . Q^T  (16 keys x 8 heads), even/odd k steps in two
+        //      accumulators to halve the dependent MMA chain
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        float sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&kw[0][kk / 4]);
+          const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&kw[1][kk / 4]);
+          const uint2 x = e4m3x4_to_f16x4(w0[kk % 4]), y = e4m3x4_to_f16x4(w1[kk % 4]);
+          mma_16816<true>((kk & 1) ? sd : sc, x.x, y.x, x.y, y.y, qb[kk][0], qb[kk][1]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[j] += sd[j];
+        uint32_t pb0, pb1;
+        softmax_step(sc, p0, pb0, pb1);
+        // ---- O^T += V^T . P^T
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
           // bytes 2dt, 2dt+1 of rows (2t, 2t+1) interleaved: (k0,d0) (k1,d0) (k0,d1) (k1,d1)
@@ -362,7 +364,38 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
           const uint2 hi = e4m3x4_to_f16x4(prmt(vw[2][dt / 2], vw[3][dt / 2], sel));
           mma_16816<true>(o[dt], lo.x, lo.y, hi.x, hi.y, pb0, pb1);
         }
-      } else {
+      }
+    } else {
+      if (ok) {
+        const uint32_t kbuf = wbase_u + st * T::kStageBytes;
+        const uint32_t vbuf = kbuf + T::kTileBytes;
+        // ---- S^T = K . Q^T  (16 keys x 8 heads), two accumulators as above
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        float sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kbuf + swz_offset(k_row, kk * 16 + k_dsub), a0, a1, a2, a3);
+          mma_16816<false>((kk & 1) ? sd : sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[j] += sd[j];
+        uint32_t pb0, pb1;
+        softmax_step(sc, p0, pb0, pb1);
+        // ---- the sequence's last, partial block: zero V rows past the context
+        if (p0 + kBlock > L) {
+          const int nvalid = L - p0;
+          uint8_t* vrow = wbase + st * T::kStageBytes + T::kTileBytes;
+          for (int e = lane; e < (kBlock - nvalid) * T::kHalves * 8; e += 32) {
+            const int r = nvalid + e / (T::kHalves * 8);
+            const int rem = e % (T::kHalves * 8);
+            *reinterpret_cast<uint4*>(vrow + (rem >> 3) * 2048 + r * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async();  // before any later TMA write to this stage
+          __syncwarp();
+        }
+        // ---- O^T += V^T . P^T
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
           uint32_t a0, a1, a2, a3;
@@ -370,12 +403,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
           mma_16816<false>(o[dt], a0, a1, a2, a3, pb0, pb1);
         }
       }
-    }
-    __syncwarp();
-    if (i + NS < nb_w) {
-      if (lane == 0) fence_proxy_async();
-      issue(i + NS);
-      ++issued;
+      __syncwarp();
+      if (i + NS < nb_w) {
+        if (lane == 0) fence_proxy_async();
+        issue(i + NS);
+        ++issued;
+      }
     }
   }
 
@@ -548,14 +581,15 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
 
 // Stages per warp: 3 x 8 KB (head_size 128) keeps 2 CTAs (8 warps, up to 16
 // blocks = 128 KB of K/V) in flight per SM.
-// FP8 stages are half the size: 4-deep rings still leave room for three CTAs
-// per SM.
+// FP8 stages are half the size: 3-deep rings leave room for four CTAs per SM
+// (16 warps), and a warp refills a stage as soon as its block is in registers.
+// (Measured on GB300 decode batches: 3 stages beat 2 and 4.)
 cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                const DecodeArgs& a, int head_size, bool fp8,
                                cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
   if (fp8) {
-    if (head_size == 128) return launch_decode_t<128, 4, true>(kmap, vmap, a, stream);
+    if (head_size == 128) return launch_decode_t<128, 3, true>(kmap, vmap, a, stream);
     return launch_decode_t<64, 6, true>(kmap, vmap, a, stream);
   }
   if (head_size == 128) return launch_decode_t<128, 3, false>(kmap, vmap, a, stream);
