@@ -165,6 +165,7 @@ class Pool:
     def admit(self, req_id) -> int:
         """take the prefix-cache hits of a new request; returns the cached tokens."""
         r = self.reqs[req_id]
+        assert not r.blocks and r.num_computed == 0, "admit once, before any allocation"
         hits = self.computed_blocks(req_id)
         self._touch(hits)
         r.blocks = list(hits)

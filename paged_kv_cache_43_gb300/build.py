@@ -1,4 +1,5 @@
-"""Builds libpkv.so (the CUDA kernels and the C ABI of include/pkv.h) in-tree.
+"""Builds libpkv.so (the CUDA kernels and the C ABI of include/pkv.h, plus the
+host block pool of include/pkv_pool.h) in-tree.
 
 nvcc compiles each translation unit for sm_103a in parallel, then links one
 shared library into ``paged_kv_cache_43_gb300/_build/``.  The CUDA runtime is
@@ -20,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libpkv.so")
 SOURCES = ["pkv_api.cu", "pkv_write.cu", "pkv_decode.cu", "pkv_prefill.cu", "pkv_prefill_tc.cu",
-           "pkv_f32.cu", "pkv_static_scratch.cu"]
+           "pkv_f32.cu", "pkv_static_scratch.cu", "pkv_pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,7 +39,7 @@ def _flags():
 
 def _deps_mtime() -> float:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "pkv.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     return max(os.path.getmtime(f) for f in files)
 
 

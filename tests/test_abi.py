@@ -8,13 +8,15 @@ import subprocess
 import pytest
 
 from paged_kv_cache_43_gb300 import build, pkv
+from paged_kv_cache_43_gb300 import pool
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pkv.h")
+POOL_HEADER = os.path.join(ROOT, "include", "pkv_pool.h")
 
 
-def _declared_functions():
-    text = open(HEADER).read()
+def _declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
 
@@ -27,13 +29,14 @@ def lib():
 
 def test_header_declares_the_binding_set():
     assert _declared_functions() == sorted(pkv.EXPORTED)
+    assert _declared_functions(POOL_HEADER) == sorted(pool.EXPORTED)
 
 
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\bT (pkv_\w+)", out))
-    for name in _declared_functions():
+    for name in _declared_functions() + _declared_functions(POOL_HEADER):
         assert name in exported, name
         assert hasattr(lib, name)
 
@@ -64,6 +67,6 @@ def test_struct_layout_matches_header(tmp_path):
 def test_header_compiles_as_c_and_cxx(tmp_path):
     for lang, comp in (("c", "gcc"), ("cpp", "g++")):
         src = tmp_path / f"inc.{lang}"
-        src.write_text('#include "pkv.h"\nint main(void){return PKV_OK;}\n')
+        src.write_text('#include "pkv.h"\n#include "pkv_pool.h"\nint main(void){return PKV_OK;}\n')
         subprocess.run([comp, "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
                         str(src), "-o", str(tmp_path / f"inc_{lang}")], check=True)

@@ -1,0 +1,70 @@
+"""The decode loop's host logic on CPU (scheduling, prefix hits, recompute
+preemption, block tables and slots from the C++ pool), with the two kernel
+calls replaced by stand-ins that record what they were given.  Checks the
+invariants the kernels rely on: slots of one step are distinct and inside
+the blocks the tables list, context_lens = last position + 1, decode rows
+lead the batch, and every request finishes with its full token count."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_43_gb300 import build, pkv
+from paged_kv_cache_43_gb300 import decode_loop as DL
+
+
+@pytest.fixture(autouse=True)
+def _stub_kernels(monkeypatch):
+    build.build()
+    calls = []
+
+    def write(k, v, slots, kc, vc, stream=None):
+        calls.append(("write", slots.clone()))
+
+    def attention(out, q, kc, vc, bt, cl, qsl, scale, **kw):
+        out.zero_()
+        calls.append(("attn", bt.clone(), cl.clone(), qsl.clone(), kw))
+
+    monkeypatch.setattr(DL.pkv, "write", write)
+    monkeypatch.setattr(DL.pkv, "attention", attention)
+    return calls
+
+
+@pytest.mark.parametrize("num_blocks,caching,window", [(96, True, 0), (14, True, 0),
+                                                        (14, False, 0), (40, True, 33)])
+def test_host_loop_invariants(_stub_kernels, num_blocks, caching, window):
+    rng = np.random.default_rng(5)
+    loop = DL.DecodeLoop(num_blocks=num_blocks, num_q_heads=4, num_kv_heads=2, head_size=64,
+                         caching=caching, window=window, max_batch_tokens=160, device="cpu")
+    system = [int(x) for x in rng.integers(0, 512, 40)]
+    want = {}
+    for i in range(8):
+        p = system + [int(x) for x in rng.integers(0, 512, int(rng.integers(3, 30)))]
+        n = int(rng.integers(5, 25))
+        want[loop.add_request(p, n)] = len(p) + n
+    finished, preempted, steps = {}, 0, 0
+    reqs = {}
+    while not loop.done():
+        st = loop.step()
+        assert st is not None
+        steps += 1
+        preempted += len(st.preempted)
+        slots = st.slot_mapping.numpy()
+        assert len(set(slots.tolist())) == len(slots)          # distinct slots in a step
+        bt = st.block_tables.numpy()
+        for i, rid in enumerate(st.req_ids):
+            pos = st.positions[i]
+            assert int(st.context_lens[i]) == pos[-1] + 1
+            q0 = int(st.query_start_loc[i])
+            for j, p in enumerate(pos):
+                assert slots[q0 + j] == bt[i, p // 16] * 16 + p % 16
+                assert bt[i, p // 16] != loop.pool.null_block
+        ql = st.q_lens
+        nd = next((i for i, x in enumerate(ql) if x != 1), len(ql))
+        assert all(x > 1 for x in ql[nd:])                      # decode rows lead
+        for rid in st.finished:
+            finished[rid] = True
+        assert steps < 1000
+    assert set(finished) == set(want)
+    if num_blocks == 14:
+        assert preempted > 0
+    assert loop.pool.num_free() == num_blocks - 1             # everything returned

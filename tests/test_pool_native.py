@@ -1,0 +1,108 @@
+"""The C++ block pool (libpkv.so, include/pkv_pool.h) against the oracle
+(oracle/pool.py) on seeded random request traces: every slot, block table,
+reference count, cached hash and the free queue's order must be identical
+after every operation (integer work: bit-exact).  Host only, no GPU."""
+import random
+
+import pytest
+
+from oracle import pool as O
+from paged_kv_cache_43_gb300 import build
+from paged_kv_cache_43_gb300 import pool as N
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+
+
+def _same_state(o, n, live, nb):
+    assert n.num_free() == o.num_free()
+    assert n.free_queue() == o.free
+    assert n.cached_blocks() == o.cached_blocks()
+    for b in range(nb):
+        assert n.block_state(b) == (o.ref[b], o.hash[b]), b
+    for rid in live:
+        assert n.block_table(rid) == o.block_table(rid)
+        assert n.num_computed(rid) == o.num_computed(rid)
+
+
+def _trace(seed, nb, caching, window, steps=400):
+    rng = random.Random(seed)
+    o, n = O.Pool(nb, caching=caching), N.BlockPool(nb, caching=caching)
+    assert n.null_block == o.null_block
+    prompts = [[rng.randrange(50) for _ in range(rng.randrange(16, 80))] for _ in range(3)]
+    live, next_id = [], 0
+    for _ in range(steps):
+        op = rng.random()
+        if op < 0.25 or not live:
+            rid = next_id
+            next_id += 1
+            base = rng.choice(prompts) if rng.random() < 0.7 else []
+            toks = base + [rng.randrange(50) for _ in range(rng.randrange(1, 40))]
+            o.add_request(rid, toks)
+            n.add_request(rid, toks)
+            assert n.admit(rid) == o.admit(rid)
+            # prefill in one or two chunks
+            todo = len(toks) - o.num_computed(rid)
+            chunk = todo if rng.random() < 0.5 else max(1, todo // 2)
+            so = o.allocate_slots(rid, chunk, window)
+            sn = n.allocate_slots(rid, chunk, window)
+            assert (sn is None) == (so is None)
+            if so is None:
+                o.free_request(rid)
+                n.free_request(rid)
+            else:
+                assert list(sn) == so
+                live.append(rid)
+        elif op < 0.8:
+            rid = rng.choice(live)
+            todo = len(o.reqs[rid].tokens) - o.num_computed(rid)
+            if todo <= 0:
+                t = rng.randrange(50)
+                o.append_token(rid, t)
+                n.append_token(rid, t)
+                todo = 1
+            so = o.allocate_slots(rid, todo, window)
+            sn = n.allocate_slots(rid, todo, window)
+            assert (sn is None) == (so is None)
+            if so is None:
+                live.remove(rid)
+                o.free_request(rid)
+                n.free_request(rid)
+            else:
+                assert list(sn) == so
+        else:
+            rid = live.pop(rng.randrange(len(live)))
+            o.free_request(rid)
+            n.free_request(rid)
+        _same_state(o, n, live, nb)
+    n.close()
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("nb,caching,window", [(24, True, 0), (64, True, 0), (24, False, 0),
+                                                (40, True, 40), (40, True, 17), (16, False, 9)])
+def test_native_pool_matches_oracle_on_random_traces(seed, nb, caching, window):
+    _trace(seed * 131 + nb, nb, caching, window)
+
+
+def test_block_tables_rows_and_errors():
+    n = N.BlockPool(20)
+    n.add_request(7, list(range(40)))
+    n.admit(7)
+    n.allocate_slots(7, 40)
+    n.add_request(9, list(range(100, 110)))
+    n.admit(9)
+    n.allocate_slots(9, 10)
+    bt = n.block_tables([7, 9], 4)
+    assert bt.tolist() == [[1, 2, 3, -1], [4, -1, -1, -1]]
+    with pytest.raises(Exception):
+        n.block_tables([7], 2)                 # row longer than the stride
+    with pytest.raises(Exception):
+        n.add_request(7, [1])                  # duplicate id
+    with pytest.raises(Exception):
+        n.admit(7)                             # admit after allocation
+    with pytest.raises(Exception):
+        n.free_request(12345)                  # unknown id
+    n.close()
