@@ -558,6 +558,82 @@ def end_to_end(kv, args, stream, device, step_bytes):
             "steps": n}
 
 
+def pool_trace(pool, steps, running=256, prompt=768, shared=512, turnover=16, seed=0):
+    """A serving trace on a block pool (the C++ one or the oracle's, same
+    interface): `running` requests whose prompts share a `shared`-token system
+    prompt decode one token per step; every 16 steps `turnover` of them finish
+    and as many new ones are admitted (prefix hits + prefill of the rest).
+    Returns (slots allocated, seconds)."""
+    rng = np.random.default_rng(seed)
+    system = [int(x) for x in rng.integers(0, 32000, shared)]
+    batched = hasattr(pool, "allocate_slots_batch")
+    live, next_id, slots = [], 0, 0
+
+    def admit():
+        nonlocal next_id, slots
+        rid = next_id
+        next_id += 1
+        toks = system + [int(x) for x in rng.integers(0, 32000, prompt - shared)]
+        pool.add_request(rid, toks)
+        cached = pool.admit(rid)
+        s = pool.allocate_slots(rid, len(toks) - cached)
+        slots += len(s)
+        live.append(rid)
+
+    t0 = time.perf_counter()
+    for _ in range(running):
+        admit()
+    for step in range(steps):
+        if batched:
+            pool.append_token_batch(live, [step] * len(live))
+        else:
+            for rid in live:
+                pool.append_token(rid, step)
+        if batched:
+            s, done = pool.allocate_slots_batch(live, [1] * len(live))
+            assert done == len(live)
+            slots += len(s)
+        else:
+            for rid in live:
+                slots += len(pool.allocate_slots(rid, 1))
+        if step % 16 == 15:
+            for _ in range(turnover):
+                pool.free_request(live.pop(0))
+                admit()
+    return slots, time.perf_counter() - t0
+
+
+def run_pool_bench(args):
+    """Host block pool on a serving trace: the C++ pool (one batched call per
+    decode step) against the oracle's Python pool on a shorter run of the same
+    trace."""
+    from paged_kv_cache_43_gb300 import build
+    from paged_kv_cache_43_gb300 import pool as P
+    import oracle.pool as OP
+    build.build()
+    steps = max(args.steps, 16)
+    n = P.BlockPool(65536, 16, True)
+    pool_trace(n, 16)                       # warm-up
+    n.close()
+    n = P.BlockPool(65536, 16, True)
+    slots, dt = pool_trace(n, steps)
+    cached = n.cached_blocks()
+    n.close()
+    o_steps = 16
+    o_slots, o_dt = pool_trace(OP.Pool(65536, 16, True), o_steps)
+    return {
+        "metric": "host block pool: slots allocated per second on a decode-loop trace",
+        "value": round(slots / dt, 1), "unit": "slots/s", "higher_is_better": True,
+        "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4),
+        "config": {"workload": "256 running requests, 768-token prompts sharing a 512-token "
+                               "system prompt, 16 finish and 16 arrive every 16 steps",
+                   "num_blocks": 65536, "block_size": 16, "cached_blocks_at_end": cached},
+        "cpu_baseline": {"value": round(o_slots / o_dt, 1), "unit": "slots/s", "cores": 1,
+                         "kind": "oracle", "sample": f"the same trace, {o_steps} steps"},
+        "data": "synthetic token ids",
+    }
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: each step is the oracle's KV write +
     attention on a bounded sample of the same workload (generated on the GPU
@@ -626,6 +702,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="override the batch size (profiling captures on a smaller case)")
+    ap.add_argument("--pool-bench", action="store_true",
+                    help="time the host block pool (C++ vs oracle) on a serving trace; no GPU")
     ap.add_argument("--profile", action="store_true",
                     help="run warmup+steps plain steps only (for ncu), print no bench line")
     args = ap.parse_args()
@@ -636,6 +714,10 @@ def main():
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local = _env_int("LOCAL_RANK", 0)
+
+    if args.pool_bench:
+        print(json.dumps(run_pool_bench(args)), flush=True)
+        return
 
     if args.impl == "reference":
         line = run_reference(args, rank, world)

@@ -64,6 +64,10 @@ int pkv_pool_add_request(pkv_pool *pool, int64_t req_id, const int32_t *tokens,
 /* Appends generated token ids to a request (copied). */
 int pkv_pool_append_tokens(pkv_pool *pool, int64_t req_id, const int32_t *tokens,
                            int32_t num_tokens);
+/* One sampled token for each of num_reqs requests (req_ids[i] gets
+ * tokens[i]), in one call.  Stops at the first unknown id (PKV_E_REQUEST). */
+int pkv_pool_append_token_batch(pkv_pool *pool, const int64_t *req_ids, const int32_t *tokens,
+                                int32_t num_reqs);
 /* Prefix-cache lookup for a request that holds no blocks yet: the hit blocks
  * become its first blocks (shared, counted) and *num_cached_tokens (a multiple
  * of block_size) tokens count as computed. */
@@ -76,6 +80,16 @@ int pkv_pool_admit(pkv_pool *pool, int64_t req_id, int32_t *num_cached_tokens);
  * the request's computed count.  PKV_POOL_NO_SPACE: nothing changed. */
 int pkv_pool_allocate_slots(pkv_pool *pool, int64_t req_id, int32_t num_new_tokens,
                             int32_t sliding_window, int64_t *slot_mapping);
+/* One scheduler step's allocations in one call: pkv_pool_allocate_slots for
+ * req_ids[i] with num_new_tokens[i], i = 0, 1, ... in order, the slots packed
+ * back to back into slot_mapping (sum of num_new_tokens entries; may be NULL).
+ * Stops at the first request the pool cannot serve; *num_done = requests
+ * served (the rest untouched).  Returns PKV_OK when all were served, else
+ * PKV_POOL_NO_SPACE or the first error. */
+int pkv_pool_allocate_slots_batch(pkv_pool *pool, const int64_t *req_ids,
+                                  const int32_t *num_new_tokens, int32_t num_reqs,
+                                  int32_t sliding_window, int64_t *slot_mapping,
+                                  int32_t *num_done);
 /* Releases every block of the request (last to first) and forgets it. */
 int pkv_pool_free_request(pkv_pool *pool, int64_t req_id);
 

@@ -186,6 +186,18 @@ int pkv_pool_append_tokens(pkv_pool* pool, int64_t req_id, const int32_t* tokens
   return PKV_OK;
 }
 
+int pkv_pool_append_token_batch(pkv_pool* pool, const int64_t* req_ids, const int32_t* tokens,
+                                int32_t num_reqs) {
+  if (!pool || (num_reqs > 0 && (!req_ids || !tokens))) return PKV_E_NULL;
+  if (num_reqs < 0) return PKV_E_SHAPE;
+  for (int32_t i = 0; i < num_reqs; ++i) {
+    auto it = pool->reqs.find(req_ids[i]);
+    if (it == pool->reqs.end()) return PKV_E_REQUEST;
+    it->second.tokens.push_back(tokens[i]);
+  }
+  return PKV_OK;
+}
+
 int pkv_pool_admit(pkv_pool* pool, int64_t req_id, int32_t* num_cached_tokens) {
   if (!pool || !num_cached_tokens) return PKV_E_NULL;
   auto it = pool->reqs.find(req_id);
@@ -259,6 +271,24 @@ int pkv_pool_allocate_slots(pkv_pool* pool, int64_t req_id, int32_t num_new_toke
         if (r.blocks[i] != pool->null_block) pool->file_block(r.blocks[i], r.hashes[i]);
       r.num_filed = n_full;
     }
+  }
+  return PKV_OK;
+}
+
+int pkv_pool_allocate_slots_batch(pkv_pool* pool, const int64_t* req_ids,
+                                  const int32_t* num_new_tokens, int32_t num_reqs,
+                                  int32_t sliding_window, int64_t* slot_mapping,
+                                  int32_t* num_done) {
+  if (!pool || !num_done || (num_reqs > 0 && (!req_ids || !num_new_tokens))) return PKV_E_NULL;
+  if (num_reqs < 0) return PKV_E_SHAPE;
+  *num_done = 0;
+  int64_t off = 0;
+  for (int32_t i = 0; i < num_reqs; ++i) {
+    const int st = pkv_pool_allocate_slots(pool, req_ids[i], num_new_tokens[i], sliding_window,
+                                           slot_mapping ? slot_mapping + off : nullptr);
+    if (st != PKV_OK) return st;
+    off += num_new_tokens[i];
+    *num_done = i + 1;
   }
   return PKV_OK;
 }

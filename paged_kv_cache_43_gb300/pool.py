@@ -13,7 +13,9 @@ NO_SPACE = 1
 E_REQUEST = -10
 EXPORTED = ("pkv_pool_create", "pkv_pool_destroy", "pkv_pool_num_free", "pkv_pool_null_block",
             "pkv_pool_num_cached", "pkv_pool_add_request", "pkv_pool_append_tokens",
-            "pkv_pool_admit", "pkv_pool_allocate_slots", "pkv_pool_free_request",
+            "pkv_pool_append_token_batch",
+            "pkv_pool_admit", "pkv_pool_allocate_slots", "pkv_pool_allocate_slots_batch",
+            "pkv_pool_free_request",
             "pkv_pool_block_table", "pkv_pool_build_block_tables", "pkv_pool_num_computed",
             "pkv_pool_block_state", "pkv_pool_free_queue")
 
@@ -34,8 +36,10 @@ def _lib():
             "pkv_pool_num_cached": (i32, [vp]),
             "pkv_pool_add_request": (ctypes.c_int, [vp, i64, P32, i32]),
             "pkv_pool_append_tokens": (ctypes.c_int, [vp, i64, P32, i32]),
+            "pkv_pool_append_token_batch": (ctypes.c_int, [vp, P64, P32, i32]),
             "pkv_pool_admit": (ctypes.c_int, [vp, i64, P32]),
             "pkv_pool_allocate_slots": (ctypes.c_int, [vp, i64, i32, i32, P64]),
+            "pkv_pool_allocate_slots_batch": (ctypes.c_int, [vp, P64, P32, i32, i32, P64, P32]),
             "pkv_pool_free_request": (ctypes.c_int, [vp, i64]),
             "pkv_pool_block_table": (ctypes.c_int, [vp, i64, P32, i32, P32]),
             "pkv_pool_build_block_tables": (ctypes.c_int, [vp, P64, i32, P32, i32]),
@@ -100,6 +104,12 @@ class BlockPool:
         a, ptr = _i32(tokens)
         self._check(self._lib.pkv_pool_append_tokens(self._p, int(req_id), ptr, a.size))
 
+    def append_token_batch(self, req_ids, tokens):
+        ids = np.ascontiguousarray(req_ids, dtype=np.int64)
+        t, tp = _i32(tokens)
+        self._check(self._lib.pkv_pool_append_token_batch(
+            self._p, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), tp, ids.size))
+
     def admit(self, req_id: int) -> int:
         n = ctypes.c_int32(0)
         self._check(self._lib.pkv_pool_admit(self._p, int(req_id), ctypes.byref(n)))
@@ -112,6 +122,18 @@ class BlockPool:
             self._p, int(req_id), int(num_new_tokens), int(window),
             out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))))
         return None if st == NO_SPACE else out[:num_new_tokens]
+
+    def allocate_slots_batch(self, req_ids, num_new_tokens, window: int = 0):
+        """(slots of the served requests, packed; number of requests served)"""
+        ids = np.ascontiguousarray(req_ids, dtype=np.int64)
+        nn = np.ascontiguousarray(num_new_tokens, dtype=np.int32)
+        out = np.empty(max(int(nn.sum()), 1), dtype=np.int64)
+        done = ctypes.c_int32(0)
+        self._check(self._lib.pkv_pool_allocate_slots_batch(
+            self._p, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            nn.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ids.size, int(window),
+            out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), ctypes.byref(done)))
+        return out[:int(nn[:done.value].sum())], int(done.value)
 
     def free_request(self, req_id: int):
         self._check(self._lib.pkv_pool_free_request(self._p, int(req_id)))

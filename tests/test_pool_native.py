@@ -106,3 +106,44 @@ def test_block_tables_rows_and_errors():
     with pytest.raises(Exception):
         n.free_request(12345)                  # unknown id
     n.close()
+
+
+def test_batch_allocation_equals_one_by_one():
+    rng = random.Random(9)
+    a, b = N.BlockPool(30), N.BlockPool(30)
+    for rid in range(6):
+        toks = [rng.randrange(50) for _ in range(rng.randrange(5, 40))]
+        for p in (a, b):
+            p.add_request(rid, toks)
+            p.admit(rid)
+    want = [rng.randrange(1, 30) for _ in range(6)]
+    slots, done = a.allocate_slots_batch(list(range(6)), want)
+    one, served = [], 0
+    for rid in range(6):
+        s = b.allocate_slots(rid, want[rid])
+        if s is None:
+            break
+        one += list(s)
+        served += 1
+    assert list(slots) == one and done == served
+    assert a.free_queue() == b.free_queue()
+    a.close()
+    b.close()
+
+
+def test_batch_append_equals_one_by_one():
+    a, b = N.BlockPool(30), N.BlockPool(30)
+    for p in (a, b):
+        for rid in range(3):
+            p.add_request(rid, [1, 2, 3])
+            p.admit(rid)
+            p.allocate_slots(rid, 3)
+    a.append_token_batch([0, 1, 2], [7, 8, 9])
+    for rid, t in zip(range(3), [7, 8, 9]):
+        b.append_token(rid, t)
+    for p in (a, b):
+        for rid in range(3):
+            p.allocate_slots(rid, 1)
+    assert [a.block_table(r) for r in range(3)] == [b.block_table(r) for r in range(3)]
+    a.close()
+    b.close()
