@@ -18,6 +18,7 @@ import torch
 import oracle
 from oracle import brute
 from paged_kv_cache_43_gb300 import workloads as W
+from tests.support import oracle_step
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -472,3 +473,23 @@ def test_fp8_attention_equals_bf16_attention_on_representable_values():
                                   A(wl.context_lens), A(wl.query_start_loc), wl.scale)
         q0, q1 = int(wl.query_start_loc[s]), int(wl.query_start_loc[s + 1])
         np.testing.assert_allclose(out8[q0:q1], ref[q0:q1], atol=1e-12, rtol=0)
+
+
+# ------------------------------------------------------- cascade
+
+@pytest.mark.parametrize("hq,hkv,pblocks", [(4, 4, 3), (8, 2, 8), (8, 1, 1)])
+def test_cascade_decomposition_equals_attention(hq, hkv, pblocks):
+    """Prefix state (shared keys) merged with the suffix state = the plain
+    attention of each decode row (ch. 6 cascade branch + merge_attn_states)."""
+    S = 6
+    rng = np.random.default_rng(hq + pblocks)
+    ctx = rng.integers(pblocks * 16 + 1, pblocks * 16 + 90, S)
+    wl = W.make_workload([1] * S, ctx, num_q_heads=hq, num_kv_heads=hkv, head_size=64,
+                         dtype=torch.float32, seed=17 + pblocks, shared_prefix_blocks=pblocks,
+                         shared_seqs=tuple(range(S)))
+    exp, _, kc, vc = oracle_step(wl)
+    A = W.as_oracle_array
+    P = oracle.Problem(A(wl.q), kc, vc, A(wl.block_tables), A(wl.context_lens),
+                       A(wl.query_start_loc), wl.scale)
+    got = oracle.cascade(P, pblocks * 16)
+    np.testing.assert_allclose(got, exp, atol=1e-12, rtol=0)
