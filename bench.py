@@ -558,6 +558,109 @@ def end_to_end(kv, args, stream, device, step_bytes):
             "steps": n}
 
 
+def _time_calls(fn, steps, warmup, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_cascade_bench(args, device):
+    """Cascade attention against the plain call on two batches whose sequences
+    share a prefix: (1) the mixed workload 4, whose first 16 decode sequences
+    share 64 blocks (cascade for those 16, pkv_attention for the rest of the
+    batch), and (2) a decode batch of 64 sequences sharing a 2048-token prefix
+    (suffixes U[128, 2048], 32 q / 8 kv heads, head_size 128).  Reports
+    attention time and GB/s over the logical bytes (every sequence's keys) and
+    over the unique bytes (the shared prefix counted once)."""
+    from paged_kv_cache_43_gb300 import build, pkv
+    from paged_kv_cache_43_gb300 import workloads as W
+    build.build()
+    pkv.load()
+    stream = torch.cuda.current_stream(device)
+    res = {}
+
+    def kv_bytes(ctx, hkv, d, e=2):
+        return int(np.asarray(ctx, np.int64).sum()) * hkv * d * e * 2
+
+    # (2) shared-prefix decode batch
+    S, P = 64, 128
+    rng = np.random.default_rng(4321)
+    ctx = P * 16 + rng.integers(128, 2048, S, endpoint=True)
+    wl = W.make_workload(np.ones(S, np.int64), ctx, num_q_heads=32, num_kv_heads=8,
+                         head_size=128, seed=4321, device=device, shared_prefix_blocks=P,
+                         shared_seqs=tuple(range(S)))
+    pkv.write(wl.k_new, wl.v_new, wl.slot_mapping, wl.k_cache, wl.v_cache)
+    out = torch.empty_like(wl.q)
+    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, max_query_len=1,
+                         max_context_len=wl.max_context_len)
+    ws = torch.empty(max(pkv.workspace_size(wl.k_cache, meta),
+                         pkv.cascade_workspace_size(wl.k_cache, meta, P)), dtype=torch.uint8,
+                     device=device)
+    plain = lambda: pkv.attention(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables,
+                                  wl.context_lens, wl.query_start_loc, wl.scale, max_query_len=1,
+                                  max_context_len=wl.max_context_len, workspace=ws)
+    casc = lambda: pkv.attention_cascade(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables,
+                                         wl.context_lens, wl.query_start_loc, wl.scale, P,
+                                         max_context_len=wl.max_context_len, workspace=ws)
+    logical = kv_bytes(ctx, 8, 128)
+    unique = kv_bytes(ctx - P * 16, 8, 128) + kv_bytes([P * 16], 8, 128)
+    for name, fn in (("plain", plain), ("cascade", casc)):
+        ms = _time_calls(fn, args.steps, args.warmup, stream)
+        res[f"shared2048_{name}"] = {"attention_ms": round(ms, 5),
+                                     "logical_GBs": round(logical / ms / 1e6, 1),
+                                     "unique_GBs": round(unique / ms / 1e6, 1)}
+    del wl, out, ws
+    # (1) workload 4: cascade for its sharing decode sequences, plain for the rest
+    wl = W.workload(4, device=device)
+    nsh = len(wl.shared_seqs)
+    Pb = wl.shared_prefix_blocks
+    pkv.write(wl.k_new, wl.v_new, wl.slot_mapping, wl.k_cache, wl.v_cache)
+    out = torch.empty_like(wl.q)
+    qsl_rest = (wl.query_start_loc[nsh:] - nsh).contiguous()
+    bt_sh, cl_sh, qsl_sh = wl.block_tables[:nsh], wl.context_lens[:nsh], wl.query_start_loc[:nsh + 1]
+    bt_rest, cl_rest = wl.block_tables[nsh:], wl.context_lens[nsh:]
+    ws = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    ws2 = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    mcl_sh = int(wl.ctx_lens[:nsh].max())
+    plain4 = lambda: pkv.attention(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables,
+                                   wl.context_lens, wl.query_start_loc, wl.scale,
+                                   max_query_len=wl.max_query_len,
+                                   max_context_len=wl.max_context_len,
+                                   num_decode_seqs=wl.num_decode_seqs, workspace=ws)
+
+    def casc4():
+        pkv.attention_cascade(out[:nsh], wl.q[:nsh], wl.k_cache, wl.v_cache, bt_sh, cl_sh, qsl_sh,
+                              wl.scale, Pb, max_context_len=mcl_sh, workspace=ws)
+        pkv.attention(out[nsh:], wl.q[nsh:], wl.k_cache, wl.v_cache, bt_rest, cl_rest, qsl_rest,
+                      wl.scale, max_query_len=wl.max_query_len,
+                      max_context_len=wl.max_context_len,
+                      num_decode_seqs=wl.num_decode_seqs - nsh, workspace=ws2)
+    attn_b, _, _ = algorithmic_bytes(wl)
+    shared_dup = (nsh - 1) * Pb * 16 * 8 * 128 * 2 * 2
+    for name, fn in (("plain", plain4), ("cascade", casc4)):
+        ms = _time_calls(fn, args.steps, args.warmup, stream)
+        res[f"mixed4_{name}"] = {"attention_ms": round(ms, 5),
+                                 "logical_GBs": round(attn_b / ms / 1e6, 1),
+                                 "unique_GBs": round((attn_b - shared_dup) / ms / 1e6, 1)}
+    if pkv.get_error(clear=True):
+        raise RuntimeError("device error word set")
+    return {"metric": "cascade attention vs pkv_attention on shared-prefix batches",
+            "unit": "ms / GB/s", "results": res,
+            "config": {"shared2048": "64 decode seqs, 2048 shared + U[128,2048] own keys, "
+                                     "32q/8kv, D=128 bf16",
+                       "mixed4": f"workload 4: cascade for its {nsh} sequences sharing {Pb} "
+                                 "blocks, pkv_attention for the rest"},
+            "steps": args.steps, "warmup": args.warmup}
+
+
 def pool_trace(pool, steps, running=256, prompt=768, shared=512, turnover=16, seed=0):
     """A serving trace on a block pool (the C++ one or the oracle's, same
     interface): `running` requests whose prompts share a `shared`-token system
@@ -702,6 +805,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="override the batch size (profiling captures on a smaller case)")
+    ap.add_argument("--cascade-bench", action="store_true",
+                    help="time cascade attention against pkv_attention on shared-prefix batches")
     ap.add_argument("--pool-bench", action="store_true",
                     help="time the host block pool (C++ vs oracle) on a serving trace; no GPU")
     ap.add_argument("--profile", action="store_true",
@@ -717,6 +822,11 @@ def main():
 
     if args.pool_bench:
         print(json.dumps(run_pool_bench(args)), flush=True)
+        return
+    if args.cascade_bench:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU")
+        print(json.dumps(run_cascade_bench(args, torch.device("cuda", 0))), flush=True)
         return
 
     if args.impl == "reference":

@@ -228,6 +228,39 @@ int pkv_attention_fp8(void *out, const void *q, const void *k_cache, const void 
                       const pkv_attn_meta *meta, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* Cascade attention ([book] ch. 6: "Structure des métadonnées", the cascade
+ * fields use_cascade / common_prefix_len; the sequence diagram, where the
+ * cascade branch runs a prefix call and a suffix call and merges them with
+ * merge_attn_states; "Réflexion de conception", the use_cascade_attention
+ * gate).  For a decode batch (every sequence one query row, max_query_len <=
+ * 1, no sliding window) whose sequences' first common_prefix_blocks
+ * block-table entries name the same physical blocks (the caller guarantees
+ * it; sequence 0's entries are read): the shared prefix keys are attended
+ * once for all rows of all sequences (K/V read once per 8 (sequence, q head)
+ * columns instead of once per sequence), each row's own keys after the prefix
+ * separately, and the partial results merged.  Same result as pkv_attention
+ * (arguments as there).  Every sequence needs L > 16 * common_prefix_blocks
+ * (else its rows are zeroed and PKV_ERR_CONTEXT_LEN set).  bf16 caches only
+ * (PKV_E_DTYPE otherwise); PKV_E_META for prefill rows, a window, or a prefix
+ * outside [1, min(block_table_stride, (max_context_len - 1) / 16)].  The
+ * workspace is required (size from the function below). */
+size_t pkv_attention_cascade_workspace_size(const pkv_cache_desc *cache,
+                                            const pkv_attn_meta *meta,
+                                            int32_t common_prefix_blocks);
+int pkv_attention_cascade(void *out, const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens,
+                          const int32_t *query_start_loc, float scale,
+                          int32_t common_prefix_blocks, const pkv_cache_desc *cache,
+                          const pkv_attn_meta *meta, void *workspace, size_t workspace_bytes,
+                          void *stream);
+/* Whether to use cascade attention, host only.  1 when the [book]'s gate
+ * passes (common prefix >= 256 tokens, >= 8 sequences, no sliding window; and,
+ * for this build, decode rows only and a prefix shorter than the longest
+ * context) and a cost rule measured on GB300 says it pays: prefix >= 1024
+ * tokens and (num_seqs - 1) * prefix tokens >= 65536 (the [book]'s own rule
+ * is a rough CTA/wave model); else 0. */
+int pkv_use_cascade(const pkv_attn_meta *meta, int32_t common_prefix_blocks);
+
 /* Reads (and, if clear != 0, resets) the current device's error word: the OR
  * of PKV_ERR_* bits raised by kernels since the last clear.  SYNCHRONISES the
  * device first.  Returns PKV_OK or PKV_E_CUDA. */

@@ -140,8 +140,7 @@ struct Plan {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan* p) {
-  if (int st = check_cache(c)) return st;
+int check_meta(const pkv_cache_desc* c, const pkv_attn_meta* m) {
   if (m == nullptr) return PKV_E_NULL;
   if (m->num_seqs < 0 || m->num_tokens < 0 || m->max_query_len < 0 || m->max_context_len < 0 ||
       m->block_table_stride < 1)
@@ -153,6 +152,29 @@ int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan
   if (m->kv_split_tokens != 0 &&
       (m->kv_split_tokens < 64 || m->kv_split_tokens > 2048 || m->kv_split_tokens % 64 != 0))
     return PKV_E_META;
+  return PKV_OK;
+}
+
+// Cache blocks per decode split (CTA).  Measured on GB300 decode batches: 1024
+// keys (512 KB of K+V per kv head at D=128) by default; 2048 for long contexts
+// (>= 16K keys), which halves the split partials and the CTAs that find
+// nothing to do, as long as that still leaves four waves of CTAs; shorter
+// chunks only when the batch has too few (sequence, head) units to fill the
+// GPU twice over.  `max_blocks`: blocks the longest row reads; `units`:
+// (sequence, kv head, 8-head group) triples.
+int choose_split_blocks(int max_blocks, int64_t units, int num_sms, int kv_split_tokens) {
+  if (kv_split_tokens > 0) return kv_split_tokens / kBlock;
+  const int64_t slots = 2LL * num_sms;  // two CTAs per SM
+  auto ctas = [&](int sb) { return units * ((max_blocks + sb - 1) / sb); };
+  int split_blocks = 64;
+  if (max_blocks * kBlock >= 16384 && ctas(128) >= 4 * slots) split_blocks = 128;
+  while (split_blocks > 4 && ctas(split_blocks) < 2 * slots) split_blocks /= 2;
+  return split_blocks;
+}
+
+int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan* p) {
+  if (int st = check_cache(c)) return st;
+  if (int st = check_meta(c, m)) return st;
   *p = Plan{};
   if (c->dtype == PKV_F32) return PKV_OK;  // one kernel, no workspace
   int nd = 0;
@@ -167,24 +189,9 @@ int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan
     const int wb = (m->sliding_window + kBlock - 1) / kBlock + 1;
     if (wb < max_blocks) max_blocks = wb;
   }
-  int split_blocks;
-  if (m->kv_split_tokens > 0) {
-    split_blocks = m->kv_split_tokens / kBlock;
-  } else {
-    // Chunk of keys per CTA, measured on GB300 decode batches: 1024 keys
-    // (512 KB of K+V per kv head at D=128) by default; 2048 for long contexts
-    // (>= 16K keys), which halves the split partials and the CTAs that find
-    // nothing to do, as long as that still leaves four waves of CTAs; shorter
-    // chunks only when the batch has too few (sequence, head) units to fill
-    // the GPU twice over.
-    const int g_sub = (m->num_q_heads / c->num_kv_heads + 7) / 8;
-    const int64_t units = static_cast<int64_t>(nd) * c->num_kv_heads * g_sub;
-    const int64_t slots = 2LL * num_sms;  // two CTAs per SM
-    auto ctas = [&](int sb) { return units * ((max_blocks + sb - 1) / sb); };
-    split_blocks = 64;
-    if (max_blocks * kBlock >= 16384 && ctas(128) >= 4 * slots) split_blocks = 128;
-    while (split_blocks > 4 && ctas(split_blocks) < 2 * slots) split_blocks /= 2;
-  }
+  const int g_sub = (m->num_q_heads / c->num_kv_heads + 7) / 8;
+  const int split_blocks = choose_split_blocks(
+      max_blocks, static_cast<int64_t>(nd) * c->num_kv_heads * g_sub, num_sms, m->kv_split_tokens);
   p->split_blocks = split_blocks;
   p->max_splits = max_blocks > 0 ? (max_blocks + split_blocks - 1) / split_blocks : 1;
   if (p->max_splits > 1) {
@@ -192,6 +199,73 @@ int make_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int num_sms, Plan
     p->ws_o_bytes = round_up(rows * c->head_size * sizeof(float), 256);
     p->ws_bytes = p->ws_o_bytes + round_up(rows * sizeof(float), 256);
   }
+  return PKV_OK;
+}
+
+// Cascade attention over a decode batch whose sequences share their first
+// P = common_prefix_blocks blocks: a prefix launch (every row against the
+// shared keys, P blocks cut into prefix_splits chunks), a suffix launch (each
+// row against its own keys after the prefix, the usual splits) and the
+// combine, which merges prefix and suffix partials.  Workspace rows hold
+// prefix_splits + suffix_max_splits partials.
+struct CascadePlan {
+  bool tc_prefix = false;    // shared keys on the tcgen05 kernel (G divides 128)
+  int prefix_tiles = 0;      // tcgen05 prefix: 128-key tiles per CTA
+  int prefix_mtiles = 0;     // tcgen05 prefix: query-row tiles
+  int prefix_blocks = 0;
+  int prefix_split_blocks = 0;
+  int prefix_splits = 0;
+  int col_groups = 0;        // 8-column groups of (sequence, q head in group) per kv head
+  int split_blocks = 0;      // suffix split size
+  int max_splits = 0;        // prefix_splits + the longest suffix's splits
+  size_t ws_o_bytes = 0;
+  size_t ws_bytes = 0;
+};
+
+int make_cascade_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int32_t prefix_blocks,
+                      int num_sms, CascadePlan* p) {
+  if (int st = check_cache(c)) return st;
+  if (c->dtype != PKV_BF16) return PKV_E_DTYPE;
+  if (int st = check_meta(c, m)) return st;
+  // decode rows only, no window, and a prefix that every query follows
+  if (m->max_query_len > 1 || m->sliding_window != 0 || prefix_blocks < 1 ||
+      prefix_blocks > m->block_table_stride ||
+      static_cast<int64_t>(prefix_blocks) * kBlock >= m->max_context_len)
+    return PKV_E_META;
+  *p = CascadePlan{};
+  p->prefix_blocks = prefix_blocks;
+  const int G = m->num_q_heads / c->num_kv_heads;
+  p->col_groups = static_cast<int>((static_cast<int64_t>(m->num_seqs) * G + 7) / 8);
+  if (prefill_tc_supported(c->head_size, G)) {
+    // tcgen05: all decode rows of a kv head in 128-row tiles, at least two
+    // 128-key tiles per CTA, about half the SMs (their partials are merged)
+    p->tc_prefix = true;
+    const int per_cta = prefill_tc_tokens_per_cta(G);
+    p->prefix_mtiles = (m->num_seqs + per_cta - 1) / per_cta;
+    const int ktiles = (prefix_blocks * kBlock + 127) / 128;
+    const int64_t units = static_cast<int64_t>(p->prefix_mtiles) * c->num_kv_heads;
+    int tiles = static_cast<int>((ktiles * units + num_sms / 2 - 1) / (num_sms / 2));
+    tiles = tiles < 2 ? 2 : (tiles > ktiles ? ktiles : tiles);
+    p->prefix_tiles = tiles;
+    p->prefix_splits = (ktiles + tiles - 1) / tiles;
+  } else {
+    // mma.sync decode kernel over 8 (sequence, head) columns per CTA: 1024-key
+    // chunks, shorter while the launch would not fill the GPU twice
+    const int64_t prefix_units = static_cast<int64_t>(c->num_kv_heads) * p->col_groups;
+    int psb = 64;
+    while (psb > 4 && prefix_units * ((prefix_blocks + psb - 1) / psb) < 4LL * num_sms) psb /= 2;
+    p->prefix_split_blocks = psb;
+    p->prefix_splits = (prefix_blocks + psb - 1) / psb;
+  }
+  const int suffix_blocks = (m->max_context_len + kBlock - 1) / kBlock - prefix_blocks;
+  const int g_sub = (G + 7) / 8;
+  p->split_blocks =
+      choose_split_blocks(suffix_blocks, static_cast<int64_t>(m->num_seqs) * c->num_kv_heads * g_sub,
+                          num_sms, m->kv_split_tokens);
+  p->max_splits = p->prefix_splits + (suffix_blocks + p->split_blocks - 1) / p->split_blocks;
+  const size_t rows = static_cast<size_t>(m->num_seqs) * m->num_q_heads * p->max_splits;
+  p->ws_o_bytes = round_up(rows * c->head_size * sizeof(float), 256);
+  p->ws_bytes = p->ws_o_bytes + round_up(rows * sizeof(float), 256);
   return PKV_OK;
 }
 
@@ -224,7 +298,7 @@ extern "C" int pkv_write(const void* k, const void* v, const int64_t* slot_mappi
   int sms;
   if (int st = device_state(&err, &sms)) return st;
   const int ebytes = cache->dtype == PKV_BF16 ? 2 : 4;
-  WriteArgs a;
+  WriteArgs a{};
   a.k = k;
   a.v = v;
   a.slot_mapping = slot_mapping;
@@ -256,7 +330,7 @@ extern "C" int pkv_write_fp8(const void* k, const void* v, const int64_t* slot_m
   int32_t* err;
   int sms;
   if (int st = device_state(&err, &sms)) return st;
-  WriteArgs a;
+  WriteArgs a{};
   a.k = k;
   a.v = v;
   a.slot_mapping = slot_mapping;
@@ -341,7 +415,7 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
   const float LOG2E = 1.4426950408889634f;
 
   if (cache->dtype == PKV_F32) {
-    F32Args a;
+    F32Args a{};
     a.out = static_cast<float*>(out);
     a.q = static_cast<const float*>(q);
     a.k_cache = static_cast<const float*>(k_cache);
@@ -370,7 +444,7 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
   const int G = meta->num_q_heads / cache->num_kv_heads;
 
   if (p.num_decode > 0) {
-    DecodeArgs d;
+    DecodeArgs d{};
     d.out = out;
     d.q = q;
     d.block_tables = block_tables;
@@ -400,7 +474,7 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
   }
   const int npf = meta->num_seqs - p.num_decode;
   if (npf > 0) {
-    PrefillArgs f;
+    PrefillArgs f{};
     f.out = out;
     f.q = q;
     f.block_tables = block_tables;
@@ -444,6 +518,133 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
 
 }  // namespace
 }  // namespace pkv
+
+extern "C" int pkv_use_cascade(const pkv_attn_meta* meta, int32_t common_prefix_blocks) {
+  // The gate the [book] gives for cascade attention: a common prefix of at
+  // least 256 tokens, at least 8 requests, no sliding window; this build's
+  // cascade also takes decode rows only.  Then, in place of the pages' rough
+  // CTA/wave model, one measured on GB300 (32 q / 8 kv heads, head_size 128,
+  // own keys U[128, 1024]): the cascade's two extra launches cost ~15-30 us,
+  // and the plain call already meets repeated prefix reads in L2, so it wins
+  // once the prefix is >= 1024 tokens and the repeated prefix keys
+  // (sequences - 1) x prefix reach 64K (1.4x at 64 x 2048, 3.0x at 64 x 8192,
+  // 1.4x at 16 x 8192; 0.6-1.0x below).
+  if (meta == nullptr) return 0;
+  const int64_t p = static_cast<int64_t>(common_prefix_blocks) * kBlock;
+  const bool pages_gate = p >= 256 && meta->num_seqs >= 8 && meta->sliding_window == 0;
+  const bool this_build = meta->max_query_len <= 1 && p < meta->max_context_len;
+  const bool pays = p >= 1024 && (static_cast<int64_t>(meta->num_seqs) - 1) * p >= 65536;
+  return pages_gate && this_build && pays ? 1 : 0;
+}
+
+extern "C" size_t pkv_attention_cascade_workspace_size(const pkv_cache_desc* cache,
+                                                       const pkv_attn_meta* meta,
+                                                       int32_t common_prefix_blocks) {
+  int32_t* err;
+  int sms;
+  if (device_state(&err, &sms) != PKV_OK) return static_cast<size_t>(-1);
+  CascadePlan p;
+  if (make_cascade_plan(cache, meta, common_prefix_blocks, sms, &p) != PKV_OK)
+    return static_cast<size_t>(-1);
+  return p.ws_bytes;
+}
+
+extern "C" int pkv_attention_cascade(void* out, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables,
+                                     const int32_t* context_lens, const int32_t* query_start_loc,
+                                     float scale, int32_t common_prefix_blocks,
+                                     const pkv_cache_desc* cache, const pkv_attn_meta* meta,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t* err;
+  int sms;
+  if (int st = device_state(&err, &sms)) return st;
+  CascadePlan p;
+  if (int st = make_cascade_plan(cache, meta, common_prefix_blocks, sms, &p)) return st;
+  if (meta->num_seqs == 0 || meta->num_tokens == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start_loc)
+    return PKV_E_NULL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u))
+    return PKV_E_ALIGN;
+  if (workspace == nullptr || workspace_bytes < p.ws_bytes) return PKV_E_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_E_ALIGN;
+  if (cache->num_blocks == 0) return PKV_E_SHAPE;
+  CUtensorMap kmap, vmap;
+  if (int e = encode_cache_map(&kmap, k_cache, *cache)) return e;
+  if (int e = encode_cache_map(&vmap, v_cache, *cache)) return e;
+  const cudaStream_t st = as_stream(stream);
+  DecodeArgs d{};
+  d.out = out;
+  d.q = q;
+  d.block_tables = block_tables;
+  d.context_lens = context_lens;
+  d.query_start_loc = query_start_loc;
+  d.ws_o = static_cast<float*>(workspace);
+  d.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ws_o_bytes);
+  d.err = err;
+  d.bt_stride = meta->block_table_stride;
+  d.num_seqs = meta->num_seqs;
+  d.num_q_heads = meta->num_q_heads;
+  d.num_kv_heads = cache->num_kv_heads;
+  d.group = meta->num_q_heads / cache->num_kv_heads;
+  d.num_blocks = cache->num_blocks;
+  d.max_splits = p.max_splits;
+  d.num_tokens = meta->num_tokens;
+  d.max_context_len = meta->max_context_len;
+  d.scale_log2 = scale * 1.4426950408889634f;
+  d.force_partial = 1;
+  d.prefix_splits = p.prefix_splits;
+  // prefix: every row against the shared keys, through sequence 0's table
+  if (p.tc_prefix) {
+    PrefillArgs f{};
+    f.out = out;
+    f.q = q;
+    f.block_tables = block_tables;
+    f.context_lens = context_lens;
+    f.query_start_loc = query_start_loc;
+    f.err = err;
+    f.bt_stride = meta->block_table_stride;
+    f.num_seqs = meta->num_seqs;
+    f.num_q_heads = meta->num_q_heads;
+    f.num_kv_heads = cache->num_kv_heads;
+    f.group = d.group;
+    f.num_blocks = cache->num_blocks;
+    f.num_mtiles = p.prefix_mtiles;
+    f.num_tokens = meta->num_tokens;
+    f.max_query_len = 1;
+    f.scale_log2 = d.scale_log2;
+    f.cascade_prefix = 1;
+    f.prefix_len = p.prefix_blocks * kBlock;
+    f.prefix_tiles = p.prefix_tiles;
+    f.max_splits = p.max_splits;
+    f.ws_o = d.ws_o;
+    f.ws_lse = d.ws_lse;
+    CUtensorMap qmap;
+    if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
+                                 cache->head_size, d.group))
+      return e;
+    if (launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, st) != cudaSuccess)
+      return PKV_E_CUDA;
+  } else {
+    DecodeArgs pa = d;
+    pa.split_blocks = p.prefix_split_blocks;
+    pa.prefix_len = p.prefix_blocks * kBlock;
+    pa.prefix_col_groups = p.col_groups;
+    if (launch_cascade_prefix_bf16(kmap, vmap, pa, cache->head_size, st) != cudaSuccess)
+      return PKV_E_CUDA;
+  }
+  // suffix: each row against its own keys after the prefix; then the merge
+  DecodeArgs sa = d;
+  sa.split_blocks = p.split_blocks;
+  sa.key_begin_blocks = p.prefix_blocks;
+  sa.split_base = p.prefix_splits;
+  if (launch_decode_bf16(kmap, vmap, sa, cache->head_size, false, st) != cudaSuccess)
+    return PKV_E_CUDA;
+  if (launch_combine_bf16(sa, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
+  return PKV_OK;
+}
 
 extern "C" int pkv_get_error(int32_t* error_bits, int clear) {
   if (error_bits == nullptr) return PKV_E_NULL;

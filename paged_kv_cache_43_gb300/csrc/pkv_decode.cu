@@ -54,7 +54,12 @@ constexpr int decode_smem_bytes() {
 }
 
 
-template <int D, int NS, bool FP8>
+// PREFIX: the cascade prefix launch.  The MMA's 8 columns are then (sequence,
+// q head) pairs of every sequence of the batch (column gc of kv head kvh is
+// sequence gc / G, q head kvh * G + gc % G), all reading the shared prefix
+// keys [0, prefix_len) through sequence 0's block table; every column writes
+// a partial.  Otherwise the columns are q heads of one sequence's query row.
+template <int D, int NS, bool FP8, bool PREFIX>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     pkv_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
@@ -76,24 +81,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int split = blockIdx.x;
-  const int s = blockIdx.z;
-  const int ngsub = (a.group + 7) >> 3;
+  const int s = PREFIX ? 0 : blockIdx.z;  // block-table row (and sequence)
+  const int ngsub = PREFIX ? a.prefix_col_groups : (a.group + 7) >> 3;
   const int kvh = blockIdx.y / ngsub;
   const int gsub = blockIdx.y - kvh * ngsub;
   const int G = a.group;
   const int Hq = a.num_q_heads;
   const bool reporter = (split == 0 && blockIdx.y == 0 && threadIdx.x == 0);
 
-  const int L = __ldg(a.context_lens + s);
-  const int q0 = __ldg(a.query_start_loc + s);
-  const int qn = __ldg(a.query_start_loc + s + 1) - q0;
-  if (qn != 1 || q0 < 0 || q0 >= a.num_tokens) {
-    if (qn != 0 && reporter) raise_error(a.err, qn == 1 ? PKV_ERR_QUERY_LEN : PKV_ERR_DECODE_QLEN);
-    return;
+  int L, q0 = 0;
+  if constexpr (PREFIX) {
+    L = a.prefix_len;
+  } else {
+    L = __ldg(a.context_lens + s);
+    q0 = __ldg(a.query_start_loc + s);
+    const int qn = __ldg(a.query_start_loc + s + 1) - q0;
+    // (cascade: the shared-prefix launch takes sequence t's query at row t)
+    if (qn != 1 || q0 < 0 || q0 >= a.num_tokens || (a.key_begin_blocks > 0 && q0 != s)) {
+      if (qn != 0 && reporter)
+        raise_error(a.err, qn == 1 ? PKV_ERR_QUERY_LEN : PKV_ERR_DECODE_QLEN);
+      return;
+    }
   }
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-  if (L < 1 || static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len) {
+  // (cascade suffix: the query must sit after the shared prefix)
+  if (L < 1 || static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len ||
+      (!PREFIX && L <= a.key_begin_blocks * kBlock)) {
     if (reporter) raise_error(a.err, PKV_ERR_CONTEXT_LEN);
+    if (PREFIX) return;
     if (split == 0) {  // zero rows for a sequence with bad metadata
       for (int i = threadIdx.x; i < 8 * D; i += NW * 32) {
         const int g = gsub * 8 + i / D;
@@ -103,9 +118,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
     return;
   }
-  // Keys the query sees: [kfirst, L) (the sliding window, if any); the splits
-  // cover the blocks of that range only.
-  const int kfirst = (a.window > 0 && L > a.window) ? L - a.window : 0;
+  // Keys the query sees: [kfirst, L) (the sliding window, if any; a cascade
+  // suffix launch starts after the shared prefix); the splits cover the blocks
+  // of that range only.
+  const int kfirst = max((a.window > 0 && L > a.window) ? L - a.window : 0,
+                         a.key_begin_blocks * kBlock);
   const int blk0 = kfirst / kBlock;
   const int nblk_seq = (L + kBlock - 1) / kBlock - blk0;
   const int nsplit = (nblk_seq + a.split_blocks - 1) / a.split_blocks;
@@ -178,11 +195,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   // d = (D/4) t + 4 kk + {0, 1, 2, 3}.
   uint32_t qb[D / 16][2];
   {
-    const int g = gsub * 8 + (lane >> 2);
-    const bool gv = g < G;
+    int g = gsub * 8 + (lane >> 2);
+    bool gv = g < G;
+    int qr = q0;
+    if constexpr (PREFIX) {  // column -> (sequence, head in group); its query row
+      const int sc = g / G;
+      g -= sc * G;
+      qr = sc < a.num_seqs ? __ldg(a.query_start_loc + sc) : -1;
+      gv = qr >= 0 && qr < a.num_tokens;
+    }
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
         static_cast<const __nv_bfloat16*>(a.q) +
-        (static_cast<int64_t>(q0) * Hq + kvh * G + (gv ? g : 0)) * D);
+        (static_cast<int64_t>(gv ? qr : 0) * Hq + kvh * G + (gv ? g : 0)) * D);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       if constexpr (FP8) {
@@ -466,12 +490,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   }
   __syncthreads();
 
-  const bool direct = (nsplit == 1);
+  const bool direct = !PREFIX && nsplit == 1 && !a.force_partial;
   for (int idx = threadIdx.x; idx < 8 * D; idx += NW * 32) {
     const int c = idx / D;
     const int d = idx - c * D;
-    const int g = gsub * 8 + c;
-    if (g >= G) continue;
+    int g = gsub * 8 + c, seq = s;
+    if constexpr (PREFIX) {
+      seq = g / G;
+      g -= seq * G;
+      if (seq >= a.num_seqs) continue;
+    } else if (g >= G) {
+      continue;
+    }
     float r = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) r += merge_f[w * 8 + c] * merge_area(w)[c * D + d];
@@ -479,7 +509,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     if (direct) {
       out[(static_cast<int64_t>(q0) * Hq + hq) * D + d] = __float2bfloat16(r);
     } else {
-      const int64_t row = (static_cast<int64_t>(s) * Hq + hq) * a.max_splits + split;
+      const int64_t row =
+          (static_cast<int64_t>(seq) * Hq + hq) * a.max_splits + a.split_base + split;
       a.ws_o[row * D + d] = r;
       if (d == 0) a.ws_lse[row] = merge_f[NW * 8 + c];
     }
@@ -507,12 +538,15 @@ __global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs 
   const int q0 = __ldg(a.query_start_loc + s);
   const int qn = __ldg(a.query_start_loc + s + 1) - q0;
   if (qn != 1 || q0 < 0 || q0 >= a.num_tokens || L < 1 ||
-      static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len)
+      static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len ||
+      L <= a.key_begin_blocks * kBlock || (a.key_begin_blocks > 0 && q0 != s))
     return;
-  const int kfirst = (a.window > 0 && L > a.window) ? L - a.window : 0;
+  const int kfirst = max((a.window > 0 && L > a.window) ? L - a.window : 0,
+                         a.key_begin_blocks * kBlock);
   const int nblk_seq = (L + kBlock - 1) / kBlock - kfirst / kBlock;
-  const int nsplit = (nblk_seq + a.split_blocks - 1) / a.split_blocks;
-  if (nsplit <= 1) return;  // the decode kernel wrote this row directly
+  // prefix partials (cascade) first, then this row's own splits
+  const int nsplit = a.prefix_splits + (nblk_seq + a.split_blocks - 1) / a.split_blocks;
+  if (nsplit <= 1 && !a.force_partial) return;  // the decode kernel wrote this row directly
   const int64_t row = (static_cast<int64_t>(s) * a.num_q_heads + hq) * a.max_splits;
   const float* lse = a.ws_lse + row;
   float M = -INFINITY;
@@ -564,15 +598,18 @@ __global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs 
         __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
 }
 
-template <int D, int NS, bool FP8>
+template <int D, int NS, bool FP8, bool PREFIX = false>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
                             const DecodeArgs& a, cudaStream_t stream) {
   constexpr int smem = decode_smem_bytes<D, NS, FP8>();
-  auto kfn = pkv_decode_bf16_kernel<D, NS, FP8>;
+  auto kfn = pkv_decode_bf16_kernel<D, NS, FP8, PREFIX>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int ngsub = (a.group + 7) / 8;
-  dim3 grid(a.max_splits, a.num_kv_heads * ngsub, a.num_seqs);
+  // prefix launch: (prefix split, kv head x column group); otherwise (split of
+  // this launch, kv head x head group, sequence)
+  const int ngsub = PREFIX ? a.prefix_col_groups : (a.group + 7) / 8;
+  dim3 grid(PREFIX ? a.prefix_splits : a.max_splits - a.split_base, a.num_kv_heads * ngsub,
+            PREFIX ? 1 : a.num_seqs);
   kfn<<<grid, kDecodeWarps * 32, smem, stream>>>(kmap, vmap, a);
   return cudaGetLastError();
 }
@@ -594,6 +631,13 @@ cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
   }
   if (head_size == 128) return launch_decode_t<128, 3, false>(kmap, vmap, a, stream);
   return launch_decode_t<64, 4, false>(kmap, vmap, a, stream);
+}
+
+cudaError_t launch_cascade_prefix_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                       const DecodeArgs& a, int head_size, cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.prefix_splits == 0) return cudaSuccess;
+  if (head_size == 128) return launch_decode_t<128, 3, false, true>(kmap, vmap, a, stream);
+  return launch_decode_t<64, 4, false, true>(kmap, vmap, a, stream);
 }
 
 cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream) {

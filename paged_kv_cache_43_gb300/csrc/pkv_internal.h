@@ -53,6 +53,13 @@ struct DecodeArgs {
   const float* k_descale;        // FP8 cache: [num_seqs_total, Hkv] (null otherwise)
   const float* v_descale;
   float scale_log2;              // scale * log2(e)
+  // Cascade attention (all zero otherwise).
+  int32_t key_begin_blocks;      // suffix launch: a sequence's keys start at this block
+  int32_t split_base;            // first workspace split slot this launch writes
+  int32_t force_partial;         // write partials even when a row has one split
+  int32_t prefix_splits;         // combine: leading split slots that hold prefix partials
+  int32_t prefix_len;            // prefix launch: the shared keys [0, prefix_len)
+  int32_t prefix_col_groups;     // prefix launch: 8-column groups per kv head
 };
 
 // Varlen causal attention over sequences [seq_begin, seq_begin + num_seqs).
@@ -77,6 +84,17 @@ struct PrefillArgs {
   const float* k_descale;        // FP8 cache: [num_seqs_total, Hkv] (null otherwise)
   const float* v_descale;
   float scale_log2;
+  // Cascade prefix launch of the tcgen05 kernel (cascade_prefix = 1): the
+  // decode rows 0 .. num_seqs - 1 (row t = sequence t) against the shared keys
+  // [0, prefix_len) of block-table row 0, prefix_tiles 128-key tiles per CTA
+  // (grid.z = prefix split); normalised fp32 partials and log2-sum-exps go to
+  // ws_o / ws_lse at split slot blockIdx.z of rows [seq, q head, max_splits].
+  int32_t cascade_prefix;
+  int32_t prefix_len;
+  int32_t prefix_tiles;
+  int32_t max_splits;
+  float* ws_o;
+  float* ws_lse;
 };
 
 // fp32 I/O: one CTA per (query row, q head), every sequence.
@@ -107,6 +125,11 @@ cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                const DecodeArgs& a, int head_size, bool fp8,
                                cudaStream_t stream);
 cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream);
+// Cascade prefix launch: every decode row of the batch (all sequences, all q
+// heads) against the shared prefix keys, read once per 8 columns; partials to
+// split slots [0, prefix_splits).
+cudaError_t launch_cascade_prefix_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                       const DecodeArgs& a, int head_size, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                 const PrefillArgs& a, int head_size, bool fp8,
                                 cudaStream_t stream);

@@ -134,7 +134,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int s = a.seq_begin + blockIdx.z;
+  // Cascade prefix launch: one "sequence" whose rows are the batch's decode
+  // rows (sequence t at row t), non-causal over the shared keys, one key split
+  // per grid.z; otherwise grid.z is the sequence.
+  const bool casc = a.cascade_prefix != 0;
+  const int s = casc ? 0 : a.seq_begin + blockIdx.z;
   const int kvh = blockIdx.y;
   const int mtile = a.num_mtiles - 1 - blockIdx.x;  // heaviest first
   const int G = a.group;
@@ -142,9 +146,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tile_toks = kTcRows / G;                // tokens per query tile
   const int toks = kTcTiles * tile_toks;            // tokens per CTA
 
-  const int L = __ldg(a.context_lens + s);
-  const int q0 = __ldg(a.query_start_loc + s);
-  const int qn = __ldg(a.query_start_loc + s + 1) - q0;
+  const int L = casc ? a.prefix_len : __ldg(a.context_lens + s);
+  const int q0 = casc ? 0 : __ldg(a.query_start_loc + s);
+  const int qn = casc ? a.num_seqs : __ldg(a.query_start_loc + s + 1) - q0;
   const int tok0 = mtile * toks;
   const bool bad_rows = qn < 0 || q0 < 0 || static_cast<int64_t>(q0) + qn > a.num_tokens;
   if (bad_rows || qn == 0 || tok0 >= qn) {
@@ -154,7 +158,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
   const bool bad_len = (L < 1 || static_cast<int64_t>(L) > a.bt_stride * kBlock);
-  if (bad_len || qn > L || qn > a.max_query_len) {
+  if (casc && bad_len) {
+    if (threadIdx.x == 0 && mtile == 0 && kvh == 0) raise_error(a.err, PKV_ERR_CONTEXT_LEN);
+    return;
+  }
+  if (!casc && (bad_len || qn > L || qn > a.max_query_len)) {
     if (threadIdx.x == 0 && mtile == 0 && kvh == 0)
       raise_error(a.err, bad_len ? PKV_ERR_CONTEXT_LEN : PKV_ERR_QUERY_LEN);
     const int nt = min(toks, qn - tok0);
@@ -167,20 +175,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int tok_last = min(tok0 + toks, qn) - 1;
   const int ntq = (tok0 + tile_toks < qn) ? 2 : 1;  // query tiles holding a valid row
-  const int pos_max = L - qn + tok_last;            // last key any row here can see
-  const int ntiles = (pos_max + kTcKeys) / kTcKeys;
+  // last key any row here can see (cascade prefix: every shared key)
+  const int pos_max = casc ? L - 1 : L - qn + tok_last;
   // With a sliding window, K/V tiles wholly before the lowest row's window
   // are never loaded (their block-table entries may hold the null block): the
-  // CTA walks tiles j0 .. ntiles-1, ring positions 0 .. n_rel-1.
+  // CTA walks tiles j0 .. ntiles-1, ring positions 0 .. n_rel-1.  A cascade
+  // prefix CTA walks its split's prefix_tiles tiles.
   const int pos_min = L - qn + tok0;
-  const int j0 = (a.window > 0 && pos_min - a.window + 1 > 0)
-                     ? (pos_min - a.window + 1) / kTcKeys : 0;
+  const int j0 = casc ? static_cast<int>(blockIdx.z) * a.prefix_tiles
+                      : ((a.window > 0 && pos_min - a.window + 1 > 0)
+                             ? (pos_min - a.window + 1) / kTcKeys : 0);
+  const int ntiles =
+      casc ? min(j0 + a.prefix_tiles, (L + kTcKeys - 1) / kTcKeys) : (pos_max + kTcKeys) / kTcKeys;
   const int n_rel = ntiles - j0;
+  if (n_rel <= 0) return;
   // First cache block holding a key some row can see; blocks before it in
   // tile j0 are not loaded (their entries may be null) and their V rows are
   // zeroed instead.
   const int lo_min = a.window > 0 ? pos_min - a.window + 1 : 0;
-  const int b_lo = lo_min > 0 ? lo_min / kBlock : 0;
+  const int b_lo = casc ? j0 * (kTcKeys / kBlock) : (lo_min > 0 ? lo_min / kBlock : 0);
   const int nblk = (pos_max + kBlock) / kBlock;
 
   const uint32_t q_full = smem_u32(&sh->q_full), drain = smem_u32(&sh->drain);
@@ -393,7 +406,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tok = tok0 + t * tile_toks + row / G;
     const int g = row % G;
     const bool valid = tok <= tok_last;
-    const int pos = L - qn + (valid ? tok : tok_last);
+    const int pos = casc ? L - 1 : L - qn + (valid ? tok : tok_last);
     const int ts = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the warpgroup
     const uint32_t b_sfull = smem_u32(&sh->s_full[t]);
     const uint32_t b_pfull = smem_u32(&sh->p_full[t]), b_pvdone = smem_u32(&sh->pv_done[t]);
@@ -503,7 +516,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pfull);
     }
-    if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
+    if (done && casc && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
+      // cascade prefix: the row's normalised partial and log2-sum-exp (in the
+      // scaled log2 domain of m_used) for the merge
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int64_t wrow = (static_cast<int64_t>(tok) * Hq + kvh * G + g) * a.max_splits +
+                           blockIdx.z;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tc::ld32(tO + c0, o);
+        tc::wait_ld();
+        if (valid) {
+          float4* dst = reinterpret_cast<float4*>(a.ws_o + wrow * D + c0);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                 __uint_as_float(o[4 * v + 2]) * inv,
+                                 __uint_as_float(o[4 * v + 3]) * inv);
+        }
+      }
+      if (valid) a.ws_lse[wrow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
+    } else if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * D;
@@ -540,7 +575,11 @@ cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const 
   auto kfn = pkv_prefill_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_mtiles, a.num_kv_heads, a.num_seqs);
+  // cascade prefix: grid.z = prefix key splits
+  const int gz = a.cascade_prefix ? (a.prefix_len + a.prefix_tiles * kTcKeys - 1) /
+                                        (a.prefix_tiles * kTcKeys)
+                                  : a.num_seqs;
+  dim3 grid(a.num_mtiles, a.num_kv_heads, gz);
   kfn<<<grid, kTcThreads, smem, stream>>>(qmap, kmap, vmap, a);
   return cudaGetLastError();
 }

@@ -26,8 +26,9 @@ ERR_QUERY_LEN = 1 << 3
 ERR_DECODE_QLEN = 1 << 4
 ERR_TIMEOUT = 1 << 5
 EXPORTED = ("pkv_write", "pkv_write_fp8", "pkv_attention_workspace_size", "pkv_attention",
-            "pkv_attention_fp8", "pkv_attention_static_scratch", "pkv_get_error",
-            "pkv_status_string")
+            "pkv_attention_fp8", "pkv_attention_static_scratch",
+            "pkv_attention_cascade_workspace_size", "pkv_attention_cascade", "pkv_use_cascade",
+            "pkv_get_error", "pkv_status_string")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -81,6 +82,15 @@ def load(path: str | None = None):
         lib.pkv_attention_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
                                           ctypes.POINTER(CacheDesc), ctypes.POINTER(AttnMeta),
                                           vp, ctypes.c_size_t, vp]
+        lib.pkv_attention_cascade_workspace_size.restype = ctypes.c_size_t
+        lib.pkv_attention_cascade_workspace_size.argtypes = [ctypes.POINTER(CacheDesc),
+                                                             ctypes.POINTER(AttnMeta), i32]
+        lib.pkv_attention_cascade.restype = ctypes.c_int
+        lib.pkv_attention_cascade.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, i32,
+                                              ctypes.POINTER(CacheDesc), ctypes.POINTER(AttnMeta),
+                                              vp, ctypes.c_size_t, vp]
+        lib.pkv_use_cascade.restype = ctypes.c_int
+        lib.pkv_use_cascade.argtypes = [ctypes.POINTER(AttnMeta), i32]
         lib.pkv_attention_static_scratch.restype = ctypes.c_int
         lib.pkv_attention_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                                      ctypes.POINTER(CacheDesc),
@@ -249,6 +259,48 @@ def attention_fp8(out, q, k_cache, v_cache, block_tables, context_lens, query_st
                                  float(scale), k_descale.data_ptr(), v_descale.data_ptr(),
                                  ctypes.byref(desc), ctypes.byref(meta), ws_ptr, ws_bytes,
                                  _stream(stream)))
+
+
+def cascade_workspace_size(k_cache, meta: AttnMeta, common_prefix_blocks: int) -> int:
+    desc = cache_desc(k_cache)
+    n = load().pkv_attention_cascade_workspace_size(ctypes.byref(desc), ctypes.byref(meta),
+                                                    int(common_prefix_blocks))
+    if n == ctypes.c_size_t(-1).value:
+        raise PkvError("invalid cascade description")
+    return int(n)
+
+
+def use_cascade(meta: AttnMeta, common_prefix_blocks: int) -> bool:
+    """The cascade gate (>= 256 shared tokens, >= 8 sequences, no window,
+    decode rows)."""
+    return bool(load().pkv_use_cascade(ctypes.byref(meta), int(common_prefix_blocks)))
+
+
+def attention_cascade(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
+                      common_prefix_blocks, *, max_context_len, kv_split_tokens=0,
+                      workspace=None, stream=None) -> None:
+    """pkv_attention_cascade: a decode batch whose sequences share their first
+    ``common_prefix_blocks`` blocks; same result as attention()."""
+    lib = load()
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n, dtype=k_cache.dtype)
+    _require(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _require(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    _require(query_start_loc, "query_start_loc", dtype=torch.int32, ndim=1)
+    meta = attn_meta(q, block_tables, context_lens, max_query_len=1,
+                     max_context_len=max_context_len, num_decode_seqs=-1,
+                     kv_split_tokens=kv_split_tokens)
+    desc = cache_desc(k_cache)
+    if workspace is None:
+        need = cascade_workspace_size(k_cache, meta, common_prefix_blocks)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(lib.pkv_attention_cascade(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(),
+                                     v_cache.data_ptr(), block_tables.data_ptr(),
+                                     context_lens.data_ptr(), query_start_loc.data_ptr(),
+                                     float(scale), int(common_prefix_blocks), ctypes.byref(desc),
+                                     ctypes.byref(meta), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
 
 
 def attention_static_scratch(out, q, k_cache, v_cache, block_tables, context_lens,

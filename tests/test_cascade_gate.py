@@ -1,0 +1,38 @@
+"""The cascade gate (pkv_use_cascade) on the host: the pages' conditions
+(>= 256 shared tokens, >= 8 sequences, no sliding window) plus this build's
+(decode rows, a key after the prefix) and the cost rule measured on GB300."""
+import pytest
+
+from paged_kv_cache_43_gb300 import build, pkv
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    pkv.load()
+
+
+def M(S, mcl, mq=1, w=0):
+    # AttnMeta(num_seqs, num_tokens, q heads, stride, max_query_len,
+    #          max_context_len, num_decode_seqs, window, split)
+    return pkv.AttnMeta(S, S, 8, 600, mq, mcl, -1, w, 0)
+
+
+@pytest.mark.parametrize("S,mcl,pblocks,want", [
+    (64, 3000, 128, True),      # 64 x 2048 shared keys (measured 1.4x)
+    (16, 9000, 512, True),      # 16 x 8192 (1.4x)
+    (256, 3000, 128, True),     # (2.0x)
+    (16, 3000, 128, False),     # 15 x 2048 < 64K: plain wins (0.99x)
+    (256, 1000, 32, False),     # prefix < 1024 tokens (1.02x)
+    (64, 1000, 32, False),      # (0.83x)
+    (7, 90000, 4096, False),    # < 8 sequences: the pages' gate
+    (64, 3000, 15, False),      # < 256 tokens: the pages' gate
+    (64, 2048, 128, False),     # no key after the prefix
+])
+def test_gate(S, mcl, pblocks, want):
+    assert pkv.use_cascade(M(S, mcl), pblocks) == want
+
+
+def test_gate_rejects_window_and_prefill_rows():
+    assert not pkv.use_cascade(M(64, 3000, w=64), 128)
+    assert not pkv.use_cascade(M(64, 3000, mq=2), 128)

@@ -1,0 +1,141 @@
+"""Cascade attention on the GPU against the oracle: a decode batch whose
+sequences share their first P blocks, the prefix attended once for all rows
+(tcgen05 kernel when the group size divides 128 — G = 1, 4, 8 here — else
+the mma.sync decode kernel over (sequence, head) columns — G = 3), each row's
+own keys after it, the partials merged.  The result must be the
+plain attention (oracle) within the bf16 tolerance, and equal pkv_attention's
+within it."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_43_gb300 import build, pkv
+from paged_kv_cache_43_gb300 import workloads as W
+from tests.support import TOL, max_err, nan_like, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    pkv.load()
+    pkv.get_error(clear=True)
+    yield
+    assert pkv.get_error(clear=True) == 0
+
+
+def _shared(S, pblocks, hq, hkv, d, lo, hi, seed, dtype=torch.bfloat16):
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(max(lo, pblocks * 16 + 1), hi, S, endpoint=True)
+    return W.make_workload([1] * S, ctx, num_q_heads=hq, num_kv_heads=hkv, head_size=d,
+                           dtype=dtype, seed=seed, shared_prefix_blocks=pblocks,
+                           shared_seqs=tuple(range(S)))
+
+
+def _cascade(wl, pblocks, **kw):
+    g = wl.to("cuda")
+    out = nan_like(g.q)
+    pkv.write(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache)
+    pkv.attention_cascade(out, g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens,
+                          g.query_start_loc, g.scale, pblocks,
+                          max_context_len=g.max_context_len, **kw)
+    torch.cuda.synchronize()
+    return g, out
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("S,hq,hkv", [(8, 8, 8), (16, 32, 8), (3, 64, 8), (40, 8, 2), (1, 4, 4),
+                                     (9, 12, 4), (200, 32, 8)])
+@pytest.mark.parametrize("pblocks", [1, 5, 64])
+def test_cascade_matches_oracle(S, hq, hkv, d, pblocks):
+    wl = _shared(S, pblocks, hq, hkv, d, 2, pblocks * 16 + 700, seed=S * 7 + pblocks + d)
+    exp, st, _, _ = oracle_step(wl)
+    assert not st.any()
+    g, out = _cascade(wl, pblocks)
+    assert max_err(out, exp) <= TOL[torch.bfloat16]
+    assert pkv.get_error() == 0
+
+
+@pytest.mark.parametrize("split", [0, 64, 256, 2048])
+def test_cascade_split_sizes_and_long_suffixes(split):
+    wl = _shared(12, 20, 32, 8, 128, 1000, 9000, seed=split + 1)
+    exp, _, _, _ = oracle_step(wl)
+    _, out = _cascade(wl, 20, kv_split_tokens=split)
+    assert max_err(out, exp) <= TOL[torch.bfloat16]
+
+
+def test_cascade_equals_plain_attention():
+    wl = _shared(24, 16, 32, 8, 128, 300, 3000, seed=5)
+    g, out_c = _cascade(wl, 16)
+    out_p = nan_like(g.q)
+    pkv.attention(out_p, g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens,
+                  g.query_start_loc, g.scale, max_query_len=1, max_context_len=g.max_context_len)
+    torch.cuda.synchronize()
+    assert float((out_c.float() - out_p.float()).abs().max()) <= 2e-2
+
+
+def test_cascade_of_workload4_sharing_sequences():
+    """The mixed workload's 16 decode sequences that share 64 blocks, as one
+    cascade call (the rest of the batch goes through pkv_attention)."""
+    wl = W.workload(4, small=False)
+    nsh = len(wl.shared_seqs)
+    sub = W.make_workload(wl.q_lens[:nsh], wl.ctx_lens[:nsh], num_q_heads=32, num_kv_heads=8,
+                          head_size=128, seed=44, shared_prefix_blocks=wl.shared_prefix_blocks,
+                          shared_seqs=tuple(range(nsh)))
+    exp, _, _, _ = oracle_step(sub)
+    _, out = _cascade(sub, wl.shared_prefix_blocks)
+    assert max_err(out, exp) <= TOL[torch.bfloat16]
+
+
+def test_cascade_row_inside_the_prefix_is_flagged_and_zeroed():
+    wl = _shared(8, 4, 8, 2, 128, 100, 400, seed=3)
+    g = wl.to("cuda")
+    pkv.write(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache)
+    cl = g.context_lens.clone()
+    cl[2] = 4 * 16                           # its query would sit inside the prefix
+    out = nan_like(g.q)
+    pkv.attention_cascade(out, g.q, g.k_cache, g.v_cache, g.block_tables, cl,
+                          g.query_start_loc, g.scale, 4, max_context_len=g.max_context_len)
+    assert pkv.get_error() == pkv.ERR_CONTEXT_LEN
+    assert float(out[2].float().abs().max()) == 0.0
+    A = W.as_oracle_array
+    exp, _, _, _ = oracle_step(wl)
+    rows = [r for r in range(8) if r != 2]
+    assert max_err(out, exp, rows=rows) <= TOL[torch.bfloat16]
+
+
+def test_cascade_host_errors():
+    lib = pkv.load()
+    wl = _shared(8, 16, 8, 2, 128, 300, 600, seed=1)
+    g = wl.to("cuda")
+    meta = pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=1,
+                         max_context_len=g.max_context_len)
+    mw = pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=1,
+                       max_context_len=g.max_context_len, sliding_window=64)
+    desc = pkv.cache_desc(g.k_cache)
+    E_META = -8
+    for bad in (pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=2,
+                              max_context_len=g.max_context_len), mw):
+        assert lib.pkv_attention_cascade_workspace_size(ctypes.byref(desc), ctypes.byref(bad),
+                                                        16) == ctypes.c_size_t(-1).value
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.zeros_like(g.q)
+    args = (out.data_ptr(), g.q.data_ptr(), g.k_cache.data_ptr(), g.v_cache.data_ptr(),
+            g.block_tables.data_ptr(), g.context_lens.data_ptr(), g.query_start_loc.data_ptr(),
+            ctypes.c_float(g.scale))
+    mq = pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=2,
+                       max_context_len=g.max_context_len)
+    assert lib.pkv_attention_cascade(*args, 16, ctypes.byref(desc), ctypes.byref(mq),
+                                     ws.data_ptr(), ws.numel(), None) == E_META
+    assert lib.pkv_attention_cascade(*args, 0, ctypes.byref(desc), ctypes.byref(meta),
+                                     ws.data_ptr(), ws.numel(), None) == E_META
+    assert lib.pkv_attention_cascade(*args, 16, ctypes.byref(desc), ctypes.byref(meta),
+                                     None, 0, None) == -5           # PKV_E_WORKSPACE
+    torch.cuda.synchronize()
+    assert pkv.get_error() == 0
