@@ -269,6 +269,12 @@ int pkv_get_error(int32_t *error_bits, int clear);
 /* Static, human-readable text for a status code. */
 const char *pkv_status_string(int status);
 
+/* The CUDA runtime error (cudaError_t as int, 0 = none yet) behind the most
+ * recent PKV_E_CUDA any call of this library returned in this process, and
+ * its text.  Host only; never synchronises. */
+int pkv_last_cuda_error(void);
+const char *pkv_last_cuda_error_string(void);
+
 #ifdef __cplusplus
 }
 #endif

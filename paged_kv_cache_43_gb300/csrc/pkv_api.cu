@@ -24,6 +24,21 @@ int g_num_sms[kMaxDevices] = {};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// The CUDA error behind the most recent PKV_E_CUDA (process-wide).
+std::atomic<int> g_last_cuda_error{0};
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error.store(static_cast<int>(e));
+  return PKV_E_CUDA;
+}
+
+// Returns PKV_E_CUDA from the enclosing function when a CUDA call fails.
+#define PKV_TRY(expr)                                   \
+  do {                                                  \
+    const cudaError_t e_ = (expr);                      \
+    if (e_ != cudaSuccess) return cuda_fail(e_);        \
+  } while (0)
+
 // Device-side address of the error word and the SM count, once per device.
 int device_state(int32_t** err, int* num_sms) {
   int dev = 0;
@@ -31,10 +46,9 @@ int device_state(int32_t** err, int* num_sms) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_err_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return PKV_E_CUDA;
+    PKV_TRY(cudaGetSymbolAddress(&p, g_error_word));
     int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return PKV_E_CUDA;
+    PKV_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     g_err_ptr[dev] = static_cast<int32_t*>(p);
     g_num_sms[dev] = sms;
   }
@@ -468,9 +482,8 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
     d.k_descale = k_descale;
     d.v_descale = v_descale;
     d.scale_log2 = scale * LOG2E;
-    if (launch_decode_bf16(kmap, vmap, d, cache->head_size, fp8, st) != cudaSuccess)
-      return PKV_E_CUDA;
-    if (launch_combine_bf16(d, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
+    PKV_TRY(launch_decode_bf16(kmap, vmap, d, cache->head_size, fp8, st));
+    PKV_TRY(launch_combine_bf16(d, cache->head_size, st));
   }
   const int npf = meta->num_seqs - p.num_decode;
   if (npf > 0) {
@@ -494,7 +507,7 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
     f.k_descale = k_descale;
     f.v_descale = v_descale;
     f.scale_log2 = scale * LOG2E;
-    if (!fp8 && prefill_tc_supported(cache->head_size, G)) {
+    if (prefill_tc_supported(cache->head_size, G) && (!fp8 || cache->head_size == 128)) {
       // tcgen05/TMEM kernel: two tiles of 128/G tokens x G heads per CTA.
       const int toks = prefill_tc_tokens_per_cta(G);
       f.num_mtiles = (meta->max_query_len + toks - 1) / toks;
@@ -502,15 +515,13 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
       if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
                                    cache->head_size, G))
         return e;
-      if (launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, st) != cudaSuccess)
-        return PKV_E_CUDA;
+      PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, st));
     } else {
       // FP8 caches, and group sizes that do not divide 128 rows: mma.sync
       // kernel, 64 rows per CTA.
       const int64_t rows = static_cast<int64_t>(meta->max_query_len) * G;
       f.num_mtiles = static_cast<int32_t>((rows + kPrefillRows - 1) / kPrefillRows);
-      if (launch_prefill_bf16(kmap, vmap, f, cache->head_size, fp8, st) != cudaSuccess)
-        return PKV_E_CUDA;
+      PKV_TRY(launch_prefill_bf16(kmap, vmap, f, cache->head_size, fp8, st));
     }
   }
   return PKV_OK;
@@ -625,24 +636,21 @@ extern "C" int pkv_attention_cascade(void* out, const void* q, const void* k_cac
     if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
                                  cache->head_size, d.group))
       return e;
-    if (launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, st) != cudaSuccess)
-      return PKV_E_CUDA;
+    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, false, st));
   } else {
     DecodeArgs pa = d;
     pa.split_blocks = p.prefix_split_blocks;
     pa.prefix_len = p.prefix_blocks * kBlock;
     pa.prefix_col_groups = p.col_groups;
-    if (launch_cascade_prefix_bf16(kmap, vmap, pa, cache->head_size, st) != cudaSuccess)
-      return PKV_E_CUDA;
+    PKV_TRY(launch_cascade_prefix_bf16(kmap, vmap, pa, cache->head_size, st));
   }
   // suffix: each row against its own keys after the prefix; then the merge
   DecodeArgs sa = d;
   sa.split_blocks = p.split_blocks;
   sa.key_begin_blocks = p.prefix_blocks;
   sa.split_base = p.prefix_splits;
-  if (launch_decode_bf16(kmap, vmap, sa, cache->head_size, false, st) != cudaSuccess)
-    return PKV_E_CUDA;
-  if (launch_combine_bf16(sa, cache->head_size, st) != cudaSuccess) return PKV_E_CUDA;
+  PKV_TRY(launch_decode_bf16(kmap, vmap, sa, cache->head_size, false, st));
+  PKV_TRY(launch_combine_bf16(sa, cache->head_size, st));
   return PKV_OK;
 }
 
@@ -651,12 +659,19 @@ extern "C" int pkv_get_error(int32_t* error_bits, int clear) {
   int32_t* err;
   int sms;
   if (int st = device_state(&err, &sms)) return st;
-  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_E_CUDA;
-  if (cudaMemcpy(error_bits, err, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return PKV_E_CUDA;
-  if (clear && cudaMemset(err, 0, sizeof(int32_t)) != cudaSuccess) return PKV_E_CUDA;
-  if (clear && cudaDeviceSynchronize() != cudaSuccess) return PKV_E_CUDA;
+  PKV_TRY(cudaDeviceSynchronize());
+  PKV_TRY(cudaMemcpy(error_bits, err, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  if (clear) {
+    PKV_TRY(cudaMemset(err, 0, sizeof(int32_t)));
+    PKV_TRY(cudaDeviceSynchronize());
+  }
   return PKV_OK;
+}
+
+extern "C" int pkv_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+extern "C" const char* pkv_last_cuda_error_string(void) {
+  return cudaGetErrorString(static_cast<cudaError_t>(g_last_cuda_error.load()));
 }
 
 extern "C" const char* pkv_status_string(int status) {

@@ -140,9 +140,10 @@ cudaError_t launch_attention_f32(const F32Args& a, cudaStream_t stream);
 bool prefill_tc_supported(int head_size, int group);
 int prefill_tc_tokens_per_tile(int group);
 int prefill_tc_tokens_per_cta(int group);
+// fp8 = true: e4m3 caches (head_size 128 only), widened to fp16 in shared memory.
 cudaError_t launch_prefill_tc(const CUtensorMap& qmap, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const PrefillArgs& a, int head_size,
-                              cudaStream_t stream);
+                              bool fp8, cudaStream_t stream);
 
 // Rows of the prefill kernel's query tile (grid.x covers ceil(q_len*G / this)).
 constexpr int kPrefillRows = 64;

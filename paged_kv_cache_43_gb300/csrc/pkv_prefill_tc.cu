@@ -34,6 +34,15 @@
 //    thread holds its whole row.
 //  * every wait is an mbarrier with a bounded spin and a CTA-wide abort flag;
 //    TMEM is freed on every path.
+//  * FP8 (e4m3) cache, head_size 128: TMA lands each tile's codes (128 keys x
+//    128 B, 128-byte swizzle) in the first half of its ring slot and warp 10
+//    (K) or 11 (V) widens them in place to fp16 in the bf16 tiles' layout
+//    (e4m3 is exact in fp16; a row's codes are read before its first fp16 half
+//    overwrites them), then marks the slot full for the MMAs;
+//    each softmax thread converts its own Q row to fp16 (a row beyond 2^14
+//    scaled by 2^-e, its scores by 2^e) and the MMAs run on fp16 operands with
+//    P in fp16.  The K descale folds into the score scale, the V descale into
+//    the output.
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
 #include "pkv_tc.cuh"
@@ -46,6 +55,9 @@ constexpr int kTcRows = 128;      // UMMA M (rows of one query tile)
 constexpr int kTcTiles = 2;       // query tiles per CTA
 constexpr int kTcKeys = 128;      // keys per K/V tile
 constexpr int kTcThreads = 320;   // load, MMA, 2 x 4 softmax warps
+constexpr int kTcThreadsFp8 = 384;  // + two warps widening e4m3 K and V tiles
+// (12 warps put 3 on each SM sub-partition, the same register cap per thread
+// as 10: the 64K-entry file split four ways, 16K / (3 x 32) = 170.)
 constexpr int kKStages = 3;       // K ring depth
 constexpr int kVStages = 2;       // V ring depth
 constexpr uint32_t kTmemCols = 512;
@@ -66,9 +78,10 @@ struct TcLayout {
 };
 
 struct TcShared {
-  uint64_t q_full, drain;
+  uint64_t q_full, drain, q_conv;
   uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+  uint64_t k_land[kKStages], v_land[kVStages];   // FP8: codes landed, not yet widened
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -118,11 +131,50 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// Widens one 128-key x 128 e4m3 tile (128-byte swizzled rows at `tile`) in
+// place into the fp16 tile layout (two 64-column halves, 16 KB apart,
+// 128-byte swizzled); all 32 lanes of the calling warp.  A batch covers 16
+// rows: a lane reads its 16-code chunk of 4 rows (4 loads in flight), and
+// only after the warp has read the whole batch does it write the batch's fp16
+// chunks (those of half 0 overwrite the same rows' codes); batches touch
+// disjoint rows.
+__device__ __forceinline__ void widen_tile_fp8(uint8_t* tile, int lane) {
+  const int c = lane & 7;           // chunk: columns 16c .. 16c + 15
+  const int j = 2 * (c & 3);        // its first 8-column chunk within the half
+  uint8_t* half = tile + (c >> 2) * (kTcKeys * 128);
+#pragma unroll 1
+  for (int b = 0; b < kTcKeys / 16; ++b) {
+    uint4 codes[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 16 * b + 4 * i + (lane >> 3);
+      codes[i] = *reinterpret_cast<const uint4*>(tile + r * 128 + ((c ^ (r & 7)) << 4));
+    }
+    uint4 lo[4], hi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 x = e4m3x4_to_f16x4(codes[i].x), y = e4m3x4_to_f16x4(codes[i].y);
+      const uint2 z = e4m3x4_to_f16x4(codes[i].z), w = e4m3x4_to_f16x4(codes[i].w);
+      lo[i] = make_uint4(x.x, x.y, y.x, y.y);
+      hi[i] = make_uint4(z.x, z.y, w.x, w.y);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 16 * b + 4 * i + (lane >> 3);
+      *reinterpret_cast<uint4*>(half + r * 128 + ((j ^ (r & 7)) << 4)) = lo[i];
+      *reinterpret_cast<uint4*>(half + r * 128 + (((j + 1) ^ (r & 7)) << 4)) = hi[i];
+    }
+  }
+  __syncwarp();
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
     pkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  static_assert(!FP8 || D == 128, "the e4m3 path widens 128-byte code rows");
   using Lt = TcLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -197,12 +249,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nblk = (pos_max + kBlock) / kBlock;
 
   const uint32_t q_full = smem_u32(&sh->q_full), drain = smem_u32(&sh->drain);
+  // the MMAs may read Q once it has landed (bf16) or been converted (FP8)
+  const uint32_t q_ready = FP8 ? smem_u32(&sh->q_conv) : q_full;
   if (threadIdx.x == 0) {
     prefetch_tensor_map(&qmap);
     prefetch_tensor_map(&kmap);
     prefetch_tensor_map(&vmap);
     mbar_init(q_full, 1);
     mbar_init(drain, 1);
+    mbar_init(smem_u32(&sh->q_conv), 8);   // one arrival per softmax warp
     for (int t = 0; t < kTcTiles; ++t) {
       mbar_init(smem_u32(&sh->s_full[t]), 1);
       mbar_init(smem_u32(&sh->p_full[t]), 4);
@@ -211,10 +266,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(smem_u32(&sh->k_full[i]), 1);
       mbar_init(smem_u32(&sh->k_empty[i]), 1);
+      mbar_init(smem_u32(&sh->k_land[i]), 1);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(smem_u32(&sh->v_full[i]), 1);
       mbar_init(smem_u32(&sh->v_empty[i]), 1);
+      mbar_init(smem_u32(&sh->v_land[i]), 1);
     }
     sh->abort = 0;
     fence_barrier_init();
@@ -257,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool in_range = blk < nblk && blk >= b_lo;
         ok[b] = in_range && bid[b] >= 0 && bid[b] < a.num_blocks;
         if (!is_v && in_range && !ok[b] && lane == 0) raise_error(a.err, PKV_ERR_BLOCK_ID);
-        bytes += ok[b] ? Lt::kHalves * 2048u : 0u;
+        bytes += ok[b] ? (FP8 ? 2048u : Lt::kHalves * 2048u) : 0u;
       }
       if (lane == 0) {
         if (bytes == 0) {
@@ -267,10 +324,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int b = 0; b < kBlocks; ++b) {
             if (!ok[b]) continue;
+            if constexpr (FP8) {  // 16 rows x 128 codes: rows b*16 .. b*16+15 of the tile
+              tma_load_3d(dst + b * 2048, is_v ? &vmap : &kmap, full, 0, kvh, bid[b] * kBlock,
+                          keep);
+            } else {
 #pragma unroll
-            for (int h = 0; h < Lt::kHalves; ++h)
-              tma_load_3d(dst + h * Lt::kKvHalf + b * 2048, is_v ? &vmap : &kmap, full, h * 64,
-                          kvh, bid[b] * kBlock, keep);
+              for (int h = 0; h < Lt::kHalves; ++h)
+                tma_load_3d(dst + h * Lt::kKvHalf + b * 2048, is_v ? &vmap : &kmap, full,
+                            h * 64, kvh, bid[b] * kBlock, keep);
+            }
           }
         }
       }
@@ -284,8 +346,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (rel >= kKStages &&
             !warp_wait(smem_u32(&sh->k_empty[st]), ((rel / kKStages) - 1) & 1, abort, a.err))
           break;
+        // (FP8: the codes land on k_land; warp 10 widens them, then k_full)
         issue_tile(it, ids_cur, false, smem_u32(sK + st * Lt::kTileBytes),
-                   smem_u32(&sh->k_full[st]));
+                   smem_u32(FP8 ? &sh->k_land[st] : &sh->k_full[st]));
       }
       if (it >= j0 + 1) {
         const int iv = it - 1;
@@ -295,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             !warp_wait(smem_u32(&sh->v_empty[st]), ((rv / kVStages) - 1) & 1, abort, a.err))
           break;
         issue_tile(iv, ids_prev, true, smem_u32(sV + st * Lt::kTileBytes),
-                   smem_u32(&sh->v_full[st]));
+                   smem_u32(FP8 ? &sh->v_land[st] : &sh->v_full[st]));
       }
       ids_prev = ids_cur;
       ids_cur = ids_next;
@@ -303,8 +366,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kTcKeys, 0, 0);
-      constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, D, 0, 1);
+      constexpr uint32_t idS = FP8 ? tc::idesc_f16_f32(kTcRows, kTcKeys, 0, 0)
+                                   : tc::idesc_bf16_f32(kTcRows, kTcKeys, 0, 0);
+      constexpr uint32_t idO = FP8 ? tc::idesc_f16_f32(kTcRows, D, 0, 1)
+                                   : tc::idesc_bf16_f32(kTcRows, D, 0, 1);
       auto issue_s = [&](int t, int j) {
         const uint32_t q_addr = smem_u32(sQ + t * Lt::kQTile);
         const uint32_t k_addr = smem_u32(sK + (j % kKStages) * Lt::kTileBytes);
@@ -336,7 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int s_next[kTcTiles] = {0, 0};   // next tile index whose S is issued
       int pv_next[kTcTiles] = {0, 0};  // next tile index whose P V is issued
       int k_released = 0, v_released = 0;  // ring stages handed back to the producer
-      bool ok = wait_or_abort(q_full, 0, abort, a.err);
+      bool ok = wait_or_abort(q_ready, 0, abort, a.err);
       uint64_t idle_since = 0;
       while (ok) {
         bool progress = false;
@@ -397,6 +462,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (void)mbar_wait(drain, 0);
     }
     __syncwarp();
+  } else if (FP8 && warp >= 10) {
+    // ------------------------------------------------- widen e4m3 tiles (FP8)
+    const bool is_v = warp == 11;
+    for (int i = 0; i < n_rel; ++i) {
+      const int st = is_v ? i % kVStages : i % kKStages;
+      const int ph = is_v ? (i / kVStages) & 1 : (i / kKStages) & 1;
+      if (!warp_wait(smem_u32(is_v ? &sh->v_land[st] : &sh->k_land[st]), ph, abort, a.err))
+        break;
+      widen_tile_fp8(is_v ? sV + st * Lt::kTileBytes : sK + st * Lt::kTileBytes, lane);
+      fence_proxy_async();   // generic writes, then the tensor core reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(is_v ? &sh->v_full[st] : &sh->k_full[st]));
+    }
   } else {
     // ------------------------------------------------------------ softmax
     const int t = (warp - 2) >> 2;                // query tile of this warpgroup
@@ -412,7 +490,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t b_pfull = smem_u32(&sh->p_full[t]), b_pvdone = smem_u32(&sh->pv_done[t]);
     const uint32_t tS = tmem + lane_off + col_s(t), tP = tmem + lane_off + col_p(t);
     const uint32_t tO = tmem + lane_off + col_o(t);
-    const float sl2 = a.scale_log2;
+    float sl2 = a.scale_log2;
+    float out_scale = 1.f;
+    if constexpr (FP8) {
+      // descales of this (sequence, kv head); this thread's Q row to fp16
+      sl2 *= __ldg(a.k_descale + static_cast<int64_t>(s) * a.num_kv_heads + kvh);
+      out_scale = __ldg(a.v_descale + static_cast<int64_t>(s) * a.num_kv_heads + kvh);
+      bool qok = warp_wait(q_full, 0, abort, a.err);
+      if (qok) {
+        uint8_t* qrow = sQ + t * Lt::kQTile + row * 128;
+        uint4 v[2 * 8];
+        float amax = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            v[h * 8 + j] = *reinterpret_cast<const uint4*>(qrow + h * Lt::kQHalf + ((j ^ (row & 7)) << 4));
+            const uint32_t w[4] = {v[h * 8 + j].x, v[h * 8 + j].y, v[h * 8 + j].z, v[h * 8 + j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+          }
+        const int ex = f16_row_exponent(amax);
+        const float down = pow2f(-ex);
+        sl2 *= pow2f(ex);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 u = v[h * 8 + j];
+            *reinterpret_cast<uint4*>(qrow + h * Lt::kQHalf + ((j ^ (row & 7)) << 4)) =
+                make_uint4(bf16x2_to_f16x2(u.x, down), bf16x2_to_f16x2(u.y, down),
+                           bf16x2_to_f16x2(u.z, down), bf16x2_to_f16x2(u.w, down));
+          }
+        fence_proxy_async();   // generic writes, then the tensor core reads
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->q_conv));
+    }
     float m_used = -INFINITY, l = 0.f;
     bool done = t < ntq;
     const int lo = a.window > 0 ? pos - a.window + 1 : 0;  // first key in this row's window
@@ -480,7 +595,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::fma_f32x2(x[k], x[k + 1], m2, b2, y0, y1);
           y0 = ex2(y0);
           y1 = ex2(y1);
-          pk[c] = pack_bf16(y0, y1);
+          pk[c] = pack2<FP8>(y0, y1);
           tc::add_f32x2(acc[c & 3], y0, y1);
         }
         tc::st32(tP + c0, pk);
@@ -540,7 +655,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (valid) a.ws_lse[wrow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
     } else if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? out_scale / l : 0.f;
       __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -568,11 +683,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                         const PrefillArgs& a, cudaStream_t stream) {
   constexpr int smem = tc_smem_bytes<D>();
-  auto kfn = pkv_prefill_tc_kernel<D>;
+  auto kfn = pkv_prefill_tc_kernel<D, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // cascade prefix: grid.z = prefix key splits
@@ -580,7 +695,7 @@ cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const 
                                         (a.prefix_tiles * kTcKeys)
                                   : a.num_seqs;
   dim3 grid(a.num_mtiles, a.num_kv_heads, gz);
-  kfn<<<grid, kTcThreads, smem, stream>>>(qmap, kmap, vmap, a);
+  kfn<<<grid, FP8 ? kTcThreadsFp8 : kTcThreads, smem, stream>>>(qmap, kmap, vmap, a);
   return cudaGetLastError();
 }
 
@@ -596,10 +711,11 @@ int prefill_tc_tokens_per_cta(int group) { return kTcTiles * kTcRows / group; }
 
 cudaError_t launch_prefill_tc(const CUtensorMap& qmap, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const PrefillArgs& a, int head_size,
-                              cudaStream_t stream) {
+                              bool fp8, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_mtiles == 0) return cudaSuccess;
-  if (head_size == 128) return launch_tc_t<128>(qmap, kmap, vmap, a, stream);
-  return launch_tc_t<64>(qmap, kmap, vmap, a, stream);
+  if (fp8) return launch_tc_t<128, true>(qmap, kmap, vmap, a, stream);
+  if (head_size == 128) return launch_tc_t<128, false>(qmap, kmap, vmap, a, stream);
+  return launch_tc_t<64, false>(qmap, kmap, vmap, a, stream);
 }
 
 }  // namespace pkv

@@ -28,7 +28,8 @@ ERR_TIMEOUT = 1 << 5
 EXPORTED = ("pkv_write", "pkv_write_fp8", "pkv_attention_workspace_size", "pkv_attention",
             "pkv_attention_fp8", "pkv_attention_static_scratch",
             "pkv_attention_cascade_workspace_size", "pkv_attention_cascade", "pkv_use_cascade",
-            "pkv_get_error", "pkv_status_string")
+            "pkv_get_error", "pkv_status_string", "pkv_last_cuda_error",
+            "pkv_last_cuda_error_string")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -99,13 +100,21 @@ def load(path: str | None = None):
         lib.pkv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_status_string.argtypes = [ctypes.c_int]
+        lib.pkv_last_cuda_error.restype = ctypes.c_int
+        lib.pkv_last_cuda_error.argtypes = []
+        lib.pkv_last_cuda_error_string.restype = ctypes.c_char_p
+        lib.pkv_last_cuda_error_string.argtypes = []
         _lib = lib
         return lib
 
 
 def _check(status: int):
     if status != 0:
-        raise PkvError(f"pkv status {status}: {load().pkv_status_string(status).decode()}")
+        lib = load()
+        msg = f"pkv status {status}: {lib.pkv_status_string(status).decode()}"
+        if status == -7:   # PKV_E_CUDA: say which CUDA error
+            msg += f" ({lib.pkv_last_cuda_error_string().decode()})"
+        raise PkvError(msg)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
