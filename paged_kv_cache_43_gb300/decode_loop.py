@@ -10,7 +10,9 @@ token budget and the pool allow, preempts the most recently admitted request
 when a decode finds no block (its blocks go back; it is re-admitted later and
 recomputes what the cache no longer holds), writes the step's K/V rows with
 pkv_write at the pool's slots and runs pkv_attention over the pool's block
-tables.
+tables — or, for a decode-only step whose requests share leading blocks and
+when pkv_use_cascade says it pays ("Implémentation du cœur ... vLLM", ch. 6:
+the scheduler's common_prefix_len feeding use_cascade), cascade attention.
 
 There is no model: a token's q, k and v rows are a fixed function of (token
 id, position) — rows of seeded N(0, 1) tables summed in fp32 and rounded to
@@ -56,13 +58,14 @@ class Step:
     positions: list = field(default_factory=list)   # per request: new positions
     preempted: list = field(default_factory=list)
     finished: list = field(default_factory=list)
+    cascade_blocks: int = 0                         # > 0: cascade over this prefix
 
 
 class DecodeLoop:
     def __init__(self, *, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_size: int,
                  dtype=torch.bfloat16, device="cuda", caching: bool = True, window: int = 0,
                  vocab: int = 512, max_pos: int = 8192, max_batch_tokens: int = 4096,
-                 seed: int = 0, scale: float | None = None):
+                 seed: int = 0, scale: float | None = None, use_cascade: bool = False):
         self.pool = BlockPool(num_blocks, 16, caching)
         self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_size
         self.dtype, self.device, self.window = dtype, torch.device(device), window
@@ -73,6 +76,7 @@ class DecodeLoop:
         self.tq, self.tk, self.tv = tab(vocab, num_q_heads), tab(vocab, num_kv_heads), tab(vocab, num_kv_heads)
         self.pq, self.pk, self.pv = tab(max_pos, num_q_heads), tab(max_pos, num_kv_heads), tab(max_pos, num_kv_heads)
         self.vocab, self.seed = vocab, seed
+        self.use_cascade = use_cascade
         shape = (num_blocks, 16, num_kv_heads, head_size)
         self.k_cache = torch.full(shape, float("nan"), dtype=dtype, device=self.device)
         self.v_cache = torch.full(shape, float("nan"), dtype=dtype, device=self.device)
@@ -177,9 +181,23 @@ class DecodeLoop:
         while nd < len(q_lens) and q_lens[nd] == 1:
             nd += 1
         pkv.write(k, v, sm, self.k_cache, self.v_cache)
-        pkv.attention(out, q, self.k_cache, self.v_cache, bt, cl, qsl, self.scale,
-                      max_query_len=max(q_lens), max_context_len=max(ctx), num_decode_seqs=nd,
-                      sliding_window=self.window)
+        casc = 0
+        if self.use_cascade and nd == len(q_lens) and self.window == 0:
+            # leading blocks every row of the step shares (the common prefix)
+            rows = self.pool.block_tables(ids, stride)
+            same = np.all(rows == rows[:1], axis=0) & (rows[0] != self.pool.null_block)
+            casc = int(np.argmin(same)) if not same.all() else stride
+            casc = min(casc, (min(ctx) - 1) // 16)   # every query after the prefix
+            meta = pkv.attn_meta(q, bt, cl, max_query_len=1, max_context_len=max(ctx))
+            if casc == 0 or not pkv.use_cascade(meta, casc):
+                casc = 0
+        if casc:
+            pkv.attention_cascade(out, q, self.k_cache, self.v_cache, bt, cl, qsl, self.scale,
+                                  casc, max_context_len=max(ctx))
+        else:
+            pkv.attention(out, q, self.k_cache, self.v_cache, bt, cl, qsl, self.scale,
+                          max_query_len=max(q_lens), max_context_len=max(ctx),
+                          num_decode_seqs=nd, sliding_window=self.window)
         # sample: every scheduled request gets its next token; finished ones leave
         finished = []
         for r, positions, _ in sched:
@@ -194,4 +212,4 @@ class DecodeLoop:
                 self.pool.free_request(r.rid)
                 self.running.remove(r)
         return Step(ids, q_lens, sm, bt, cl, qsl, q, k, v, out, [s[1] for s in sched],
-                    preempted, finished)
+                    preempted, finished, casc)

@@ -86,3 +86,33 @@ def test_decode_loop_preempts_and_recomputes():
 def test_decode_loop_with_sliding_window(window):
     rows, _, loop = _run(num_blocks=64, caching=False, window=window)
     assert len(rows) > 100
+
+
+def test_decode_loop_takes_cascade_on_a_long_shared_prompt():
+    """70 requests behind a 1104-token system prompt: after the first prefill
+    the others hit the prefix cache, and their decode steps share 69 blocks,
+    which passes pkv_use_cascade; every step still matches the oracle."""
+    rng = np.random.default_rng(8)
+    loop = DecodeLoop(num_blocks=70 * 72 + 200, num_q_heads=32, num_kv_heads=8, head_size=128,
+                      caching=True, max_batch_tokens=20000, seed=8, max_pos=2048,
+                      use_cascade=True)
+    system = [int(x) for x in rng.integers(0, 512, 69 * 16)]
+    for _ in range(70):
+        loop.add_request(system + [int(x) for x in rng.integers(0, 512, int(rng.integers(3, 12)))],
+                         max_new_tokens=4)
+    A = W.as_oracle_array
+    kc, vc = A(loop.k_cache).copy(), A(loop.v_cache).copy()
+    used = 0
+    while not loop.done():
+        st = loop.step()
+        assert st is not None
+        torch.cuda.synchronize()
+        assert pkv.get_error() == 0
+        used += st.cascade_blocks > 0
+        assert oracle.write(A(st.k_new), A(st.v_new), A(st.slot_mapping), kc, vc) == 0
+        exp, status = oracle.attention(A(st.q), kc, vc, A(st.block_tables), A(st.context_lens),
+                                       A(st.query_start_loc), loop.scale)
+        assert not status.any()
+        got = st.out.float().cpu().numpy().astype(np.float64)
+        assert np.abs(got - exp).max() <= 2e-2
+    assert used >= 2
