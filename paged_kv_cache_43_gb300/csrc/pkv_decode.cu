@@ -312,6 +312,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     pb1 = movmatrix_trans(pk1);
   };
 
+  // FP8: this lane's fragment offsets inside a block's code tiles (the same
+  // for every block): K rows r0, r0 + 8 at chunks (D/64) t + c; V rows 2t,
+  // 2t+1, 2t+8, 2t+9 at the lane's D/8 bytes (see the loop below).
+  constexpr int KC = D / 64;
+  uint32_t koff[2][KC], voff[4];
+  if constexpr (FP8) {
+    const int t = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int c = 0; c < KC; ++c) koff[h][c] = swz8<D>(r0 + 8 * h, KC * t + c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int row = 2 * t + (q & 1) + 8 * (q >> 1);
+      voff[q] = D == 128 ? swz8<D>(row, r0) : swz8<D>(row, r0 >> 1) + 8 * (r0 & 1);
+    }
+  }
+
   for (int i = 0; i < nb_w; ++i) {
     const int st = i % NS;
     const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
@@ -327,7 +345,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       // above).  V: rows 2t, 2t+1, 2t+8, 2t+9, bytes [(D/8) r0, (D/8) r0 +
       // D/8): the PV output rows of step dt are d = (D/8) r0 + 2 dt + {0, 1},
       // a permutation of d undone in the merge.
-      constexpr int KC = D / 64;  // 16-byte K chunks per lane and row
       constexpr int VW = D / 32;  // 32-bit V words per lane and row
       const int t = lane & 3;
       uint4 kw[2][KC];
@@ -338,23 +355,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int c = 0; c < KC; ++c)
-            kw[h][c] = *reinterpret_cast<const uint4*>(kt + swz8<D>(r0 + 8 * h, KC * t + c));
+          for (int c = 0; c < KC; ++c) kw[h][c] = *reinterpret_cast<const uint4*>(kt + koff[h][c]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int row = 2 * t + (q & 1) + 8 * (q >> 1);
           if constexpr (D == 128) {
-            const uint4 u = *reinterpret_cast<const uint4*>(vt + swz8<D>(row, r0));
+            const uint4 u = *reinterpret_cast<const uint4*>(vt + voff[q]);
             vw[q][0] = u.x; vw[q][1] = u.y; vw[q][2] = u.z; vw[q][3] = u.w;
           } else {
-            const uint2 u = *reinterpret_cast<const uint2*>(vt + swz8<D>(row, r0 >> 1) +
-                                                            8 * (r0 & 1));
+            const uint2 u = *reinterpret_cast<const uint2*>(vt + voff[q]);
             vw[q][0] = u.x; vw[q][1] = u.y;
           }
-          if (p0 + row >= L) {  // past the context: stale codes, NaN included
+        }
+        if (p0 + kBlock > L) {  // the last block: rows past the context hold stale codes
 #pragma unroll
-            for (int w = 0; w < VW; ++w) vw[q][w] = 0u;
-          }
+          for (int q = 0; q < 4; ++q)
+            if (p0 + 2 * t + (q & 1) + 8 * (q >> 1) >= L) {
+#pragma unroll
+              for (int w = 0; w < VW; ++w) vw[q][w] = 0u;
+            }
         }
       }
       __syncwarp();
