@@ -512,7 +512,8 @@ def spot_check(wl, out, spot, window=0):
 def end_to_end(kv, args, stream, device, step_bytes):
     """Same metric through the public calls with host-resident step inputs:
     pinned H2D of q, new K/V, slots and metadata (and the descales of an e4m3
-    cache), the step, D2H of out."""
+    cache), the step, D2H of out.  The step's inputs sit in one pinned staging
+    buffer and go over in one copy; the calls take views of its device twin."""
     from paged_kv_cache_43_gb300 import pkv
     wl = kv.wl
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
@@ -520,11 +521,21 @@ def end_to_end(kv, args, stream, device, step_bytes):
     src = {n: getattr(wl, n) for n in names}
     if kv.fp8:
         src.update(k_descale=kv.kd, v_descale=kv.vd)
-    host = {n: t.cpu().pin_memory() for n, t in src.items()}
-    dev = {n: torch.empty_like(t) for n, t in src.items()}
+    offs, total = {}, 0
+    for n, t in src.items():
+        nbytes = t.numel() * t.element_size()
+        offs[n] = (total, nbytes)
+        total += (nbytes + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=device)
+    for n, t in src.items():
+        o, nb = offs[n]
+        host_buf[o:o + nb].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+    dev = {n: dev_buf[o:o + nb].view(src[n].dtype).view(src[n].shape)
+           for n, (o, nb) in offs.items()}
     out_h = torch.empty(wl.q.shape, dtype=wl.q.dtype).pin_memory()
     out_d = torch.empty_like(wl.q)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(nb for _, nb in offs.values())
     d2h = out_h.numel() * out_h.element_size()
     meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **kv.meta_kw)
     ws = torch.empty(max(pkv.workspace_size(kv.k, meta), 1), dtype=torch.uint8,
@@ -532,8 +543,7 @@ def end_to_end(kv, args, stream, device, step_bytes):
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            for n in host:
-                dev[n].copy_(host[n], non_blocking=True)
+            dev_buf.copy_(host_buf, non_blocking=True)
         kv.write(dev["k_new"], dev["v_new"], dev["slot_mapping"], stream)
         kv.attention(out_d, dev["q"], dev["block_tables"], dev["context_lens"],
                      dev["query_start_loc"], ws, stream, kd=dev.get("k_descale"),
