@@ -139,3 +139,33 @@ def test_cascade_host_errors():
                                      None, 0, None) == -5           # PKV_E_WORKSPACE
     torch.cuda.synchronize()
     assert pkv.get_error() == 0
+
+
+def test_cascade_captured_in_a_cuda_graph_replays_correctly():
+    wl = _shared(24, 16, 32, 8, 128, 300, 3000, seed=6)
+    exp, _, _, _ = oracle_step(wl)
+    g = wl.to("cuda")
+    meta = pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=1,
+                         max_context_len=g.max_context_len)
+    ws = torch.empty(pkv.cascade_workspace_size(g.k_cache, meta, 16), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(g.q)
+    s = torch.cuda.Stream()
+
+    def step():
+        pkv.write(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache, stream=s)
+        pkv.attention_cascade(out, g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens,
+                              g.query_start_loc, g.scale, 16, max_context_len=g.max_context_len,
+                              workspace=ws, stream=s)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert max_err(out, exp) <= TOL[torch.bfloat16]
+    assert pkv.get_error() == 0

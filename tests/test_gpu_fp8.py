@@ -269,3 +269,38 @@ def test_fp8_host_argument_errors():
                              ctypes.byref(d8), None) == E_NULL
     torch.cuda.synchronize()
     assert pkv.get_error() == 0
+
+
+def test_fp8_step_captured_in_a_cuda_graph_replays_correctly():
+    """Quantising write + e4m3 attention (decode split-K, combine and the
+    tcgen05 prefill with its widening warps) captured once and replayed."""
+    wl = W.workload(4, small=True)
+    g = wl.to("cuda")
+    ks, vs, kd, vd = fp8_scale_tensors(g.num_kv_heads, g.num_seqs, 11)
+    kc8, vc8 = gpu_fp8_caches(g, ks, vs)
+    exp, _, _, _ = oracle_step_fp8(wl, ks, vs, kd, vd)
+    meta = pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=g.max_query_len,
+                         max_context_len=g.max_context_len, num_decode_seqs=g.num_decode_seqs,
+                         kv_split_tokens=128)
+    ws = torch.empty(max(pkv.workspace_size(kc8, meta), 1), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(g.q)
+    s = torch.cuda.Stream()
+
+    def step():
+        pkv.write_fp8(g.k_new, g.v_new, g.slot_mapping, kc8, vc8, ks, vs, stream=s)
+        pkv.attention_fp8(out, g.q, kc8, vc8, g.block_tables, g.context_lens,
+                          g.query_start_loc, g.scale, kd, vd, max_query_len=g.max_query_len,
+                          max_context_len=g.max_context_len, num_decode_seqs=g.num_decode_seqs,
+                          kv_split_tokens=128, workspace=ws, stream=s)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert max_err(out, exp) <= TOL_FP8
+    assert pkv.get_error() == 0
