@@ -243,7 +243,8 @@ int pkv_attention_fp8(void *out, const void *q, const void *k_cache, const void 
  * (else its rows are zeroed and PKV_ERR_CONTEXT_LEN set).  bf16 caches only
  * (PKV_E_DTYPE otherwise); PKV_E_META for prefill rows, a window, or a prefix
  * outside [1, min(block_table_stride, (max_context_len - 1) / 16)].  The
- * workspace is required (size from the function below). */
+ * workspace is required (size from the function below).  e4m3 caches:
+ * pkv_attention_cascade_fp8 (PKV_E_DTYPE here). */
 size_t pkv_attention_cascade_workspace_size(const pkv_cache_desc *cache,
                                             const pkv_attn_meta *meta,
                                             int32_t common_prefix_blocks);
@@ -253,6 +254,19 @@ int pkv_attention_cascade(void *out, const void *q, const void *k_cache, const v
                           int32_t common_prefix_blocks, const pkv_cache_desc *cache,
                           const pkv_attn_meta *meta, void *workspace, size_t workspace_bytes,
                           void *stream);
+/* Cascade attention over e4m3 caches: as pkv_attention_cascade with the
+ * descales of pkv_attention_fp8 (fp32 [num_seqs, num_kv_heads], device; each
+ * row uses its own sequence's descales, the shared keys included).  The shared
+ * keys run on the tcgen05 kernel, so head_size must be 128 and the group size
+ * divide 128 (PKV_E_SHAPE otherwise); workspace size from
+ * pkv_attention_cascade_workspace_size with the e4m3 cache descriptor. */
+int pkv_attention_cascade_fp8(void *out, const void *q, const void *k_cache,
+                              const void *v_cache, const int32_t *block_tables,
+                              const int32_t *context_lens, const int32_t *query_start_loc,
+                              float scale, int32_t common_prefix_blocks, const float *k_descale,
+                              const float *v_descale, const pkv_cache_desc *cache,
+                              const pkv_attn_meta *meta, void *workspace, size_t workspace_bytes,
+                              void *stream);
 /* Whether to use cascade attention, host only.  1 when the [book]'s gate
  * passes (common prefix >= 256 tokens, >= 8 sequences, no sliding window; and,
  * for this build, decode rows only and a prefix shorter than the longest

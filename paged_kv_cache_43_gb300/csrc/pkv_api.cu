@@ -239,7 +239,7 @@ struct CascadePlan {
 int make_cascade_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int32_t prefix_blocks,
                       int num_sms, CascadePlan* p) {
   if (int st = check_cache(c)) return st;
-  if (c->dtype != PKV_BF16) return PKV_E_DTYPE;
+  if (c->dtype != PKV_BF16 && c->dtype != PKV_FP8_E4M3) return PKV_E_DTYPE;
   if (int st = check_meta(c, m)) return st;
   // decode rows only, no window, and a prefix that every query follows
   if (m->max_query_len > 1 || m->sliding_window != 0 || prefix_blocks < 1 ||
@@ -250,6 +250,9 @@ int make_cascade_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int32_t p
   p->prefix_blocks = prefix_blocks;
   const int G = m->num_q_heads / c->num_kv_heads;
   p->col_groups = static_cast<int>((static_cast<int64_t>(m->num_seqs) * G + 7) / 8);
+  // e4m3 caches: the shared keys only on the widening tcgen05 kernel
+  if (c->dtype == PKV_FP8_E4M3 && !(c->head_size == 128 && prefill_tc_supported(128, G)))
+    return PKV_E_SHAPE;
   if (prefill_tc_supported(c->head_size, G)) {
     // tcgen05: all decode rows of a kv head in 128-row tiles, at least two
     // 128-key tiles per CTA, about half the SMs (their partials are merged)
@@ -560,12 +563,62 @@ extern "C" size_t pkv_attention_cascade_workspace_size(const pkv_cache_desc* cac
   return p.ws_bytes;
 }
 
+namespace pkv {
+namespace {
+
+int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* context_lens,
+                 const int32_t* query_start_loc, float scale, int32_t common_prefix_blocks,
+                 const float* k_descale, const float* v_descale, const pkv_cache_desc* cache,
+                 const pkv_attn_meta* meta, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+}  // namespace
+}  // namespace pkv
+
 extern "C" int pkv_attention_cascade(void* out, const void* q, const void* k_cache,
                                      const void* v_cache, const int32_t* block_tables,
                                      const int32_t* context_lens, const int32_t* query_start_loc,
                                      float scale, int32_t common_prefix_blocks,
                                      const pkv_cache_desc* cache, const pkv_attn_meta* meta,
                                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (cache != nullptr && cache->dtype == PKV_FP8_E4M3) return PKV_E_DTYPE;  // _fp8 variant
+  return cascade_impl(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                      scale, common_prefix_blocks, nullptr, nullptr, cache, meta, workspace,
+                      workspace_bytes, stream);
+}
+
+extern "C" int pkv_attention_cascade_fp8(void* out, const void* q, const void* k_cache,
+                                         const void* v_cache, const int32_t* block_tables,
+                                         const int32_t* context_lens,
+                                         const int32_t* query_start_loc, float scale,
+                                         int32_t common_prefix_blocks, const float* k_descale,
+                                         const float* v_descale, const pkv_cache_desc* cache,
+                                         const pkv_attn_meta* meta, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (cache == nullptr) return PKV_E_NULL;
+  if (cache->dtype != PKV_FP8_E4M3) return PKV_E_DTYPE;
+  if (meta != nullptr && meta->num_seqs > 0 && meta->num_tokens > 0) {
+    if (!k_descale || !v_descale) return PKV_E_NULL;
+    if ((reinterpret_cast<uintptr_t>(k_descale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_descale) & 3u))
+      return PKV_E_ALIGN;
+  }
+  return cascade_impl(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                      scale, common_prefix_blocks, k_descale, v_descale, cache, meta, workspace,
+                      workspace_bytes, stream);
+}
+
+namespace pkv {
+namespace {
+
+int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* context_lens,
+                 const int32_t* query_start_loc, float scale, int32_t common_prefix_blocks,
+                 const float* k_descale, const float* v_descale, const pkv_cache_desc* cache,
+                 const pkv_attn_meta* meta, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  const bool fp8 = cache != nullptr && cache->dtype == PKV_FP8_E4M3;
   int32_t* err;
   int sms;
   if (int st = device_state(&err, &sms)) return st;
@@ -605,6 +658,8 @@ extern "C" int pkv_attention_cascade(void* out, const void* q, const void* k_cac
   d.num_tokens = meta->num_tokens;
   d.max_context_len = meta->max_context_len;
   d.scale_log2 = scale * 1.4426950408889634f;
+  d.k_descale = k_descale;
+  d.v_descale = v_descale;
   d.force_partial = 1;
   d.prefix_splits = p.prefix_splits;
   // prefix: every row against the shared keys, through sequence 0's table
@@ -632,11 +687,13 @@ extern "C" int pkv_attention_cascade(void* out, const void* q, const void* k_cac
     f.max_splits = p.max_splits;
     f.ws_o = d.ws_o;
     f.ws_lse = d.ws_lse;
+    f.k_descale = k_descale;
+    f.v_descale = v_descale;
     CUtensorMap qmap;
     if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
                                  cache->head_size, d.group))
       return e;
-    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, false, st));
+    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, st));
   } else {
     DecodeArgs pa = d;
     pa.split_blocks = p.prefix_split_blocks;
@@ -649,10 +706,13 @@ extern "C" int pkv_attention_cascade(void* out, const void* q, const void* k_cac
   sa.split_blocks = p.split_blocks;
   sa.key_begin_blocks = p.prefix_blocks;
   sa.split_base = p.prefix_splits;
-  PKV_TRY(launch_decode_bf16(kmap, vmap, sa, cache->head_size, false, st));
+  PKV_TRY(launch_decode_bf16(kmap, vmap, sa, cache->head_size, fp8, st));
   PKV_TRY(launch_combine_bf16(sa, cache->head_size, st));
   return PKV_OK;
 }
+
+}  // namespace
+}  // namespace pkv
 
 extern "C" int pkv_get_error(int32_t* error_bits, int clear) {
   if (error_bits == nullptr) return PKV_E_NULL;

@@ -493,9 +493,11 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
     float sl2 = a.scale_log2;
     float out_scale = 1.f;
     if constexpr (FP8) {
-      // descales of this (sequence, kv head); this thread's Q row to fp16
-      sl2 *= __ldg(a.k_descale + static_cast<int64_t>(s) * a.num_kv_heads + kvh);
-      out_scale = __ldg(a.v_descale + static_cast<int64_t>(s) * a.num_kv_heads + kvh);
+      // descales of this (sequence, kv head) -- a cascade prefix row's own
+      // sequence (row tok = sequence tok); this thread's Q row to fp16
+      const int ds = casc ? (valid ? tok : tok_last) : s;
+      sl2 *= __ldg(a.k_descale + static_cast<int64_t>(ds) * a.num_kv_heads + kvh);
+      out_scale = __ldg(a.v_descale + static_cast<int64_t>(ds) * a.num_kv_heads + kvh);
       bool qok = warp_wait(q_full, 0, abort, a.err);
       if (qok) {
         uint8_t* qrow = sQ + t * Lt::kQTile + row * 128;
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
       // cascade prefix: the row's normalised partial and log2-sum-exp (in the
       // scaled log2 domain of m_used) for the merge
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? out_scale / l : 0.f;
       const int64_t wrow = (static_cast<int64_t>(tok) * Hq + kvh * G + g) * a.max_splits +
                            blockIdx.z;
 #pragma unroll 1

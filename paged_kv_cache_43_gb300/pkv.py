@@ -27,7 +27,8 @@ ERR_DECODE_QLEN = 1 << 4
 ERR_TIMEOUT = 1 << 5
 EXPORTED = ("pkv_write", "pkv_write_fp8", "pkv_attention_workspace_size", "pkv_attention",
             "pkv_attention_fp8", "pkv_attention_static_scratch",
-            "pkv_attention_cascade_workspace_size", "pkv_attention_cascade", "pkv_use_cascade",
+            "pkv_attention_cascade_workspace_size", "pkv_attention_cascade",
+            "pkv_attention_cascade_fp8", "pkv_use_cascade",
             "pkv_get_error", "pkv_status_string", "pkv_last_cuda_error",
             "pkv_last_cuda_error_string")
 STATIC_SCRATCH_BYTES = 64 << 20
@@ -90,6 +91,11 @@ def load(path: str | None = None):
         lib.pkv_attention_cascade.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, i32,
                                               ctypes.POINTER(CacheDesc), ctypes.POINTER(AttnMeta),
                                               vp, ctypes.c_size_t, vp]
+        lib.pkv_attention_cascade_fp8.restype = ctypes.c_int
+        lib.pkv_attention_cascade_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, i32,
+                                                  vp, vp, ctypes.POINTER(CacheDesc),
+                                                  ctypes.POINTER(AttnMeta), vp, ctypes.c_size_t,
+                                                  vp]
         lib.pkv_use_cascade.restype = ctypes.c_int
         lib.pkv_use_cascade.argtypes = [ctypes.POINTER(AttnMeta), i32]
         lib.pkv_attention_static_scratch.restype = ctypes.c_int
@@ -310,6 +316,43 @@ def attention_cascade(out, q, k_cache, v_cache, block_tables, context_lens, quer
                                      ctypes.byref(meta), workspace.data_ptr(),
                                      workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
+
+
+def attention_cascade_fp8(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                          scale, common_prefix_blocks, k_descale, v_descale, *, max_context_len,
+                          kv_split_tokens=0, workspace=None, stream=None) -> None:
+    """pkv_attention_cascade_fp8: attention_cascade over e4m3 caches with the
+    descales of attention_fp8."""
+    lib = load()
+    for t, n in ((out, "out"), (q, "q")):
+        _require(t, n, dtype=torch.bfloat16)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n)
+        if t.dtype not in FP8_DTYPES:
+            raise PkvError(f"{n} must hold e4m3 codes (uint8 or float8_e4m3fn)")
+    _require(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _require(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    _require(query_start_loc, "query_start_loc", dtype=torch.int32, ndim=1)
+    for t, n in ((k_descale, "k_descale"), (v_descale, "v_descale")):
+        _require(t, n, dtype=torch.float32, ndim=2)
+        if tuple(t.shape) != (context_lens.shape[0], k_cache.shape[2]):
+            raise PkvError(f"{n} must be [num_seqs, num_kv_heads]")
+    meta = attn_meta(q, block_tables, context_lens, max_query_len=1,
+                     max_context_len=max_context_len, num_decode_seqs=-1,
+                     kv_split_tokens=kv_split_tokens)
+    desc = cache_desc(k_cache)
+    if workspace is None:
+        need = cascade_workspace_size(k_cache, meta, common_prefix_blocks)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(lib.pkv_attention_cascade_fp8(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(),
+                                         v_cache.data_ptr(), block_tables.data_ptr(),
+                                         context_lens.data_ptr(), query_start_loc.data_ptr(),
+                                         float(scale), int(common_prefix_blocks),
+                                         k_descale.data_ptr(), v_descale.data_ptr(),
+                                         ctypes.byref(desc), ctypes.byref(meta),
+                                         workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
 
 
 def attention_static_scratch(out, q, k_cache, v_cache, block_tables, context_lens,

@@ -169,3 +169,52 @@ def test_cascade_captured_in_a_cuda_graph_replays_correctly():
     torch.cuda.synchronize()
     assert max_err(out, exp) <= TOL[torch.bfloat16]
     assert pkv.get_error() == 0
+
+
+# ------------------------------------------------------------ e4m3 caches
+
+@pytest.mark.parametrize("S,hq,hkv,pblocks", [(8, 8, 8, 1), (16, 32, 8, 5), (40, 8, 2, 64),
+                                              (200, 32, 8, 5), (3, 64, 8, 16)])
+def test_cascade_fp8_matches_oracle(S, hq, hkv, pblocks):
+    """Descales drawn per (sequence, kv head): every row, the shared keys
+    included, must use its own sequence's."""
+    from tests.support import fp8_scale_tensors, gpu_fp8_caches, oracle_step_fp8
+    wl = _shared(S, pblocks, hq, hkv, 128, 2, pblocks * 16 + 700, seed=S + pblocks)
+    g = wl.to("cuda")
+    ks, vs, _, _ = fp8_scale_tensors(hkv, S, 13)
+    rng = np.random.default_rng(S * 3 + pblocks)
+    kd = torch.from_numpy(rng.uniform(0.002, 0.03, (S, hkv)).astype(np.float32)).cuda()
+    vd = torch.from_numpy(rng.uniform(0.005, 0.04, (S, hkv)).astype(np.float32)).cuda()
+    kc8, vc8 = gpu_fp8_caches(g, ks, vs)
+    pkv.write_fp8(g.k_new, g.v_new, g.slot_mapping, kc8, vc8, ks, vs)
+    out = nan_like(g.q)
+    pkv.attention_cascade_fp8(out, g.q, kc8, vc8, g.block_tables, g.context_lens,
+                              g.query_start_loc, g.scale, pblocks, kd, vd,
+                              max_context_len=g.max_context_len)
+    torch.cuda.synchronize()
+    exp, st, _, _ = oracle_step_fp8(wl, ks, vs, kd, vd)
+    assert not st.any()
+    assert max_err(out, exp) <= TOL[torch.bfloat16]
+    assert pkv.get_error() == 0
+
+
+def test_cascade_fp8_shapes_without_the_tcgen05_prefix_are_refused():
+    lib = pkv.load()
+    for hq, hkv, d in ((8, 8, 64), (12, 4, 128)):          # head_size 64; group 3
+        wl = _shared(8, 4, hq, hkv, d, 100, 300, seed=2)
+        g = wl.to("cuda")
+        kc8 = torch.zeros(g.k_cache.shape, dtype=torch.uint8, device="cuda")
+        meta = pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=1,
+                             max_context_len=g.max_context_len)
+        desc = pkv.cache_desc(kc8)
+        assert lib.pkv_attention_cascade_workspace_size(ctypes.byref(desc), ctypes.byref(meta),
+                                                        4) == ctypes.c_size_t(-1).value
+        with pytest.raises(pkv.PkvError):
+            kd = torch.ones((8, hkv), dtype=torch.float32, device="cuda")
+            pkv.attention_cascade_fp8(torch.zeros_like(g.q), g.q, kc8, kc8, g.block_tables,
+                                      g.context_lens, g.query_start_loc, g.scale, 4, kd, kd,
+                                      max_context_len=g.max_context_len,
+                                      workspace=torch.empty(1 << 20, dtype=torch.uint8,
+                                                            device="cuda"))
+    torch.cuda.synchronize()
+    assert pkv.get_error() == 0
