@@ -627,7 +627,23 @@ def run_cascade_bench(args, device):
         res[f"shared2048_{name}"] = {"attention_ms": round(ms, 5),
                                      "logical_GBs": round(logical / ms / 1e6, 1),
                                      "unique_GBs": round(unique / ms / 1e6, 1)}
-    del wl, out, ws
+    # the same batch over e4m3 caches (history quantised by pkv_write_fp8, untimed)
+    kc = KVCache(wl, True, 4321, 0, 0)
+    kc.write(wl.k_new, wl.v_new, wl.slot_mapping, stream)
+    plain8 = lambda: pkv.attention_fp8(out, wl.q, kc.k, kc.v, wl.block_tables, wl.context_lens,
+                                       wl.query_start_loc, wl.scale, kc.kd, kc.vd,
+                                       max_query_len=1, max_context_len=wl.max_context_len,
+                                       workspace=ws)
+    casc8 = lambda: pkv.attention_cascade_fp8(out, wl.q, kc.k, kc.v, wl.block_tables,
+                                              wl.context_lens, wl.query_start_loc, wl.scale, P,
+                                              kc.kd, kc.vd, max_context_len=wl.max_context_len,
+                                              workspace=ws)
+    for name, fn in (("plain", plain8), ("cascade", casc8)):
+        ms = _time_calls(fn, args.steps, args.warmup, stream)
+        res[f"shared2048_e4m3_{name}"] = {"attention_ms": round(ms, 5),
+                                          "logical_GBs": round(logical / 2 / ms / 1e6, 1),
+                                          "unique_GBs": round(unique / 2 / ms / 1e6, 1)}
+    del wl, out, ws, kc
     # (1) workload 4: cascade for its sharing decode sequences, plain for the rest
     wl = W.workload(4, device=device)
     nsh = len(wl.shared_seqs)
@@ -665,7 +681,7 @@ def run_cascade_bench(args, device):
     return {"metric": "cascade attention vs pkv_attention on shared-prefix batches",
             "unit": "ms / GB/s", "results": res,
             "config": {"shared2048": "64 decode seqs, 2048 shared + U[128,2048] own keys, "
-                                     "32q/8kv, D=128 bf16",
+                                     "32q/8kv, D=128 bf16 (and e4m3: GB/s over 1-byte codes)",
                        "mixed4": f"workload 4: cascade for its {nsh} sequences sharing {Pb} "
                                  "blocks, pkv_attention for the rest"},
             "steps": args.steps, "warmup": args.warmup}

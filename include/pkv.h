@@ -21,6 +21,16 @@
  *     stream).  Calls only enqueue work: they never allocate device memory,
  *     never synchronise and never copy device data to the host, so they may be
  *     captured into a CUDA graph.
+ *   - The first call on a device (with it current) also creates the
+ *     library's side stream there (non-blocking, the device's greatest
+ *     priority) and two events; make that first call before any stream
+ *     capture.  An attention call whose batch has both decode and prefill
+ *     rows enqueues its prefill launch on the side stream, forked from
+ *     `stream` by an event after the work already on `stream` and joined
+ *     back to `stream` before the call returns, so that work enqueued on
+ *     `stream` afterwards sees the whole result, inside a graph capture too.
+ *     A side stream that another thread's capture holds is not used (the
+ *     call then runs on `stream` alone).
  *   - A call returns PKV_OK or a negative PKV_E_* for a host-side argument
  *     error, in which case nothing was enqueued.  PKV_E_CUDA means a launch
  *     failed; cudaGetLastError() holds the reason.

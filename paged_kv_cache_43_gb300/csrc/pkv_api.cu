@@ -24,6 +24,21 @@ int g_num_sms[kMaxDevices] = {};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// Per device: the stream a mixed batch's prefill launch runs on while its
+// decode launches run on the caller's stream, created once at the device's
+// greatest priority (so that the block scheduler hands freed SMs to the
+// prefill tiles first and the short decode CTAs fill the prefill's tail), and
+// the events that fork it from the caller's stream and join it back.  `mu`
+// keeps the record-wait-launch-record-wait sequence of one call from
+// interleaving with another thread's.  side == nullptr: not available (the
+// launches then stay on the caller's stream).
+struct SideStream {
+  std::mutex mu;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+
 // The CUDA error behind the most recent PKV_E_CUDA (process-wide).
 std::atomic<int> g_last_cuda_error{0};
 
@@ -39,8 +54,28 @@ int cuda_fail(cudaError_t e) {
     if (e_ != cudaSuccess) return cuda_fail(e_);        \
   } while (0)
 
-// Device-side address of the error word and the SM count, once per device.
-int device_state(int32_t** err, int* num_sms) {
+void make_side_stream(SideStream* s) {
+  int least = 0, greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return;
+  cudaStream_t st = nullptr;
+  cudaEvent_t f = nullptr, j = nullptr;
+  if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) == cudaSuccess &&
+      cudaEventCreateWithFlags(&f, cudaEventDisableTiming) == cudaSuccess &&
+      cudaEventCreateWithFlags(&j, cudaEventDisableTiming) == cudaSuccess) {
+    s->side = st;
+    s->fork = f;
+    s->join = j;
+    return;
+  }
+  if (j) cudaEventDestroy(j);
+  if (f) cudaEventDestroy(f);
+  if (st) cudaStreamDestroy(st);
+  cudaGetLastError();
+}
+
+// Device-side address of the error word and the SM count, once per device
+// (with the device's side stream).
+int device_state(int32_t** err, int* num_sms, int* device = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_E_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -49,12 +84,30 @@ int device_state(int32_t** err, int* num_sms) {
     PKV_TRY(cudaGetSymbolAddress(&p, g_error_word));
     int sms = 0;
     PKV_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    make_side_stream(&g_side[dev]);
     g_err_ptr[dev] = static_cast<int32_t*>(p);
     g_num_sms[dev] = sms;
   }
   *err = g_err_ptr[dev];
   *num_sms = g_num_sms[dev];
+  if (device) *device = dev;
   return PKV_OK;
+}
+
+// Whether work may be forked from `st` onto the side stream: the side stream
+// is idle (not part of any capture), or it already belongs to the capture
+// that `st` is in.  A side stream held by another thread's capture is left
+// alone.
+bool side_usable(cudaStream_t side, cudaStream_t st) {
+  cudaStreamCaptureStatus ss = cudaStreamCaptureStatusNone, cs = cudaStreamCaptureStatusNone;
+  unsigned long long sid = 0, cid = 0;
+  if (cudaStreamGetCaptureInfo(side, &ss, &sid) != cudaSuccess ||
+      cudaStreamGetCaptureInfo(st, &cs, &cid) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (ss == cudaStreamCaptureStatusNone) return cs != cudaStreamCaptureStatusInvalidated;
+  return ss == cudaStreamCaptureStatusActive && cs == cudaStreamCaptureStatusActive && sid == cid;
 }
 
 int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
@@ -412,8 +465,8 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
                    const pkv_attn_meta* meta, void* workspace, size_t workspace_bytes,
                    void* stream) {
   int32_t* err;
-  int sms;
-  if (int st = device_state(&err, &sms)) return st;
+  int sms, dev;
+  if (int st = device_state(&err, &sms, &dev)) return st;
   Plan p;
   if (int st = make_plan(cache, meta, sms, &p)) return st;
   if (meta->num_seqs == 0 || meta->num_tokens == 0) return PKV_OK;
@@ -460,7 +513,8 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
   if (int e = encode_cache_map(&vmap, v_cache, *cache)) return e;
   const int G = meta->num_q_heads / cache->num_kv_heads;
 
-  if (p.num_decode > 0) {
+  const int npf = meta->num_seqs - p.num_decode;
+  auto decode_part = [&](cudaStream_t st) -> int {
     DecodeArgs d{};
     d.out = out;
     d.q = q;
@@ -487,9 +541,9 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
     d.scale_log2 = scale * LOG2E;
     PKV_TRY(launch_decode_bf16(kmap, vmap, d, cache->head_size, fp8, st));
     PKV_TRY(launch_combine_bf16(d, cache->head_size, st));
-  }
-  const int npf = meta->num_seqs - p.num_decode;
-  if (npf > 0) {
+    return PKV_OK;
+  };
+  auto prefill_part = [&](cudaStream_t st) -> int {
     PrefillArgs f{};
     f.out = out;
     f.q = q;
@@ -526,8 +580,37 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
       f.num_mtiles = static_cast<int32_t>((rows + kPrefillRows - 1) / kPrefillRows);
       PKV_TRY(launch_prefill_bf16(kmap, vmap, f, cache->head_size, fp8, st));
     }
+    return PKV_OK;
+  };
+  if (p.num_decode == 0) return prefill_part(st);
+  if (npf == 0) return decode_part(st);
+  // Decode and prefill rows in one batch: the prefill launch goes first, on
+  // the device's high-priority side stream forked from the caller's stream,
+  // and the decode launches follow on the caller's stream, so that the short
+  // decode CTAs fill the SMs that the prefill's last wave leaves idle; the
+  // side stream is joined back before the call returns.  (Measured on GB300,
+  // the mixed 48-decode + 4 x 512-token-chunk batch of 32 q / 8 kv heads:
+  // attention 170 us in one stream, 143 us forked.)
+  SideStream& ss = g_side[dev];
+  std::unique_lock<std::mutex> fork_lock;
+  cudaStream_t pst = st;
+  if (ss.side != nullptr) {
+    fork_lock = std::unique_lock<std::mutex>(ss.mu);
+    if (side_usable(ss.side, st)) {
+      PKV_TRY(cudaEventRecord(ss.fork, st));
+      PKV_TRY(cudaStreamWaitEvent(ss.side, ss.fork, 0));
+      pst = ss.side;
+    }
   }
-  return PKV_OK;
+  int rc = prefill_part(pst);
+  if (rc == PKV_OK) rc = decode_part(st);
+  if (pst != st) {
+    // joined after a failed launch too, so that a capture stays well formed
+    cudaError_t e = cudaEventRecord(ss.join, pst);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss.join, 0);
+    if (rc == PKV_OK && e != cudaSuccess) rc = cuda_fail(e);
+  }
+  return rc;
 }
 
 }  // namespace
