@@ -5,6 +5,7 @@
 // pkv_get_error(), which is documented as synchronising.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -229,6 +230,13 @@ int check_meta(const pkv_cache_desc* c, const pkv_attn_meta* m) {
 // chunks only when the batch has too few (sequence, head) units to fill the
 // GPU twice over.  `max_blocks`: blocks the longest row reads; `units`:
 // (sequence, kv head, 8-head group) triples.
+// Then the longest row's splits are evened out: their number is its blocks
+// over that size rounded to nearest rather than up, each ceil(blocks / n)
+// long and at most 128 (the kernel's 32 blocks per warp).  A 1024-key window
+// spans 65 blocks: one split of 65, not 64 + 1, which would also cost a
+// merge pass (measured on GB300 with 1024-key windows: 146 -> 141 us on the
+// 64 x 32-head batch, 112 -> 104 us on 256 x 8 kv heads, 27 -> 20 us on
+// 16 x 8 kv heads).
 int choose_split_blocks(int max_blocks, int64_t units, int num_sms, int kv_split_tokens) {
   if (kv_split_tokens > 0) return kv_split_tokens / kBlock;
   const int64_t slots = 2LL * num_sms;  // two CTAs per SM
@@ -236,6 +244,13 @@ int choose_split_blocks(int max_blocks, int64_t units, int num_sms, int kv_split
   int split_blocks = 64;
   if (max_blocks * kBlock >= 16384 && ctas(128) >= 4 * slots) split_blocks = 128;
   while (split_blocks > 4 && ctas(split_blocks) < 2 * slots) split_blocks /= 2;
+  if (max_blocks > 0) {
+    constexpr int kMaxSplitBlocks = 128;
+    int n = (max_blocks + split_blocks / 2) / split_blocks;
+    n = std::max(n, (max_blocks + kMaxSplitBlocks - 1) / kMaxSplitBlocks);
+    n = std::max(n, 1);
+    split_blocks = (max_blocks + n - 1) / n;
+  }
   return split_blocks;
 }
 
