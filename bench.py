@@ -462,7 +462,10 @@ def run_pkv(args, rank, world, device):
         "attention_ms": round(attn_ms, 5),
         "write_ms": round(write_ms, 5),
         "roofline": {
-            "kernel": "pkv_attention (split-K decode kernel + combine), CUDA events per call",
+            "kernel": ("pkv_attention (split-K decode kernel + combine), CUDA events per call"
+                       if wl.num_decode_seqs == wl.num_seqs else
+                       "pkv_attention (tcgen05 prefill on the side stream with the split-K "
+                       "decode kernel + combine), CUDA events per call on the caller's stream"),
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
             "traffic": traffic,
