@@ -24,10 +24,11 @@
  *   - The first call on a device (with it current) also creates the
  *     library's side stream there (non-blocking, the device's greatest
  *     priority) and two events; make that first call before any stream
- *     capture.  An attention call whose batch has both decode and prefill
- *     rows enqueues its prefill launch on the side stream, forked from
+ *     capture.  pkv_attention(_fp8/_static_scratch) on a batch with both
+ *     decode and prefill rows enqueues its prefill launch, and the cascade
+ *     calls their shared-prefix launch, on the side stream, forked from
  *     `stream` by an event after the work already on `stream` and joined
- *     back to `stream` before the call returns, so that work enqueued on
+ *     back to `stream` before the call's last launch, so that work enqueued on
  *     `stream` afterwards sees the whole result, inside a graph capture too.
  *     A side stream that another thread's capture holds is not used (the
  *     call then runs on `stream` alone).
@@ -280,8 +281,8 @@ int pkv_attention_cascade_fp8(void *out, const void *q, const void *k_cache,
 /* Whether to use cascade attention, host only.  1 when the [book]'s gate
  * passes (common prefix >= 256 tokens, >= 8 sequences, no sliding window; and,
  * for this build, decode rows only and a prefix shorter than the longest
- * context) and a cost rule measured on GB300 says it pays: prefix >= 1024
- * tokens and (num_seqs - 1) * prefix tokens >= 65536 (the [book]'s own rule
+ * context) and a cost rule measured on GB300 says it pays: prefix >= 512
+ * tokens and (num_seqs - 1) * prefix tokens >= 16384 (the [book]'s own rule
  * is a rough CTA/wave model); else 0. */
 int pkv_use_cascade(const pkv_attn_meta *meta, int32_t common_prefix_blocks);
 

@@ -111,6 +111,42 @@ bool side_usable(cudaStream_t side, cudaStream_t st) {
   return ss == cudaStreamCaptureStatusActive && cs == cudaStreamCaptureStatusActive && sid == cid;
 }
 
+// Fork-join around the device's side stream.  begin() makes the side stream
+// wait for the work already on `st` and holds the side stream's lock;
+// stream() is then where the forked launches go (the side stream, or `st`
+// itself when the side stream is missing or held by another capture); join()
+// makes `st` wait for them.  The destructor joins too (error paths), so a
+// capture on `st` never ends with unjoined work.
+class SideFork {
+ public:
+  SideFork(int dev, cudaStream_t st) : ss_(g_side[dev]), st_(st), pst_(st) {}
+  SideFork(const SideFork&) = delete;
+  SideFork& operator=(const SideFork&) = delete;
+  ~SideFork() { (void)join(); }
+  int begin() {
+    if (ss_.side == nullptr) return PKV_OK;
+    lock_ = std::unique_lock<std::mutex>(ss_.mu);
+    if (!side_usable(ss_.side, st_)) return PKV_OK;
+    PKV_TRY(cudaEventRecord(ss_.fork, st_));
+    PKV_TRY(cudaStreamWaitEvent(ss_.side, ss_.fork, 0));
+    pst_ = ss_.side;
+    return PKV_OK;
+  }
+  cudaStream_t stream() const { return pst_; }
+  int join() {
+    if (pst_ == st_) return PKV_OK;
+    pst_ = st_;
+    cudaError_t e = cudaEventRecord(ss_.join, ss_.side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st_, ss_.join, 0);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+  }
+
+ private:
+  SideStream& ss_;
+  cudaStream_t st_, pst_;
+  std::unique_lock<std::mutex> lock_;
+};
+
 int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_encode == nullptr) {
@@ -606,26 +642,12 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
   // side stream is joined back before the call returns.  (Measured on GB300,
   // the mixed 48-decode + 4 x 512-token-chunk batch of 32 q / 8 kv heads:
   // attention 170 us in one stream, 143 us forked.)
-  SideStream& ss = g_side[dev];
-  std::unique_lock<std::mutex> fork_lock;
-  cudaStream_t pst = st;
-  if (ss.side != nullptr) {
-    fork_lock = std::unique_lock<std::mutex>(ss.mu);
-    if (side_usable(ss.side, st)) {
-      PKV_TRY(cudaEventRecord(ss.fork, st));
-      PKV_TRY(cudaStreamWaitEvent(ss.side, ss.fork, 0));
-      pst = ss.side;
-    }
-  }
-  int rc = prefill_part(pst);
+  SideFork fork(dev, st);
+  if (int e = fork.begin()) return e;
+  int rc = prefill_part(fork.stream());
   if (rc == PKV_OK) rc = decode_part(st);
-  if (pst != st) {
-    // joined after a failed launch too, so that a capture stays well formed
-    cudaError_t e = cudaEventRecord(ss.join, pst);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss.join, 0);
-    if (rc == PKV_OK && e != cudaSuccess) rc = cuda_fail(e);
-  }
-  return rc;
+  const int jr = fork.join();
+  return rc != PKV_OK ? rc : jr;
 }
 
 }  // namespace
@@ -636,16 +658,17 @@ extern "C" int pkv_use_cascade(const pkv_attn_meta* meta, int32_t common_prefix_
   // least 256 tokens, at least 8 requests, no sliding window; this build's
   // cascade also takes decode rows only.  Then, in place of the pages' rough
   // CTA/wave model, one measured on GB300 (32 q / 8 kv heads, head_size 128,
-  // own keys U[128, 1024]): the cascade's two extra launches cost ~15-30 us,
-  // and the plain call already meets repeated prefix reads in L2, so it wins
-  // once the prefix is >= 1024 tokens and the repeated prefix keys
-  // (sequences - 1) x prefix reach 64K (1.4x at 64 x 2048, 3.0x at 64 x 8192,
-  // 1.4x at 16 x 8192; 0.6-1.0x below).
+  // own keys U[128, 1024]; the prefix launch on the side stream beside the
+  // suffix launch): the plain call already meets repeated prefix reads in L2,
+  // so the cascade wins once the prefix is >= 512 tokens and the repeated
+  // prefix keys (sequences - 1) x prefix reach 16K (1.09x at 64 x 512, 1.17x
+  // at 16 x 2048, 1.19x at 8 x 8192, 3.6x at 64 x 8192, 6.0x at 256 x 8192;
+  // 0.83-0.96x below, and at every 256-token prefix).
   if (meta == nullptr) return 0;
   const int64_t p = static_cast<int64_t>(common_prefix_blocks) * kBlock;
   const bool pages_gate = p >= 256 && meta->num_seqs >= 8 && meta->sliding_window == 0;
   const bool this_build = meta->max_query_len <= 1 && p < meta->max_context_len;
-  const bool pays = p >= 1024 && (static_cast<int64_t>(meta->num_seqs) - 1) * p >= 65536;
+  const bool pays = p >= 512 && (static_cast<int64_t>(meta->num_seqs) - 1) * p >= 16384;
   return pages_gate && this_build && pays ? 1 : 0;
 }
 
@@ -718,8 +741,8 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
                  void* stream) {
   const bool fp8 = cache != nullptr && cache->dtype == PKV_FP8_E4M3;
   int32_t* err;
-  int sms;
-  if (int st = device_state(&err, &sms)) return st;
+  int sms, dev;
+  if (int st = device_state(&err, &sms, &dev)) return st;
   CascadePlan p;
   if (int st = make_cascade_plan(cache, meta, common_prefix_blocks, sms, &p)) return st;
   if (meta->num_seqs == 0 || meta->num_tokens == 0) return PKV_OK;
@@ -760,6 +783,13 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
   d.v_descale = v_descale;
   d.force_partial = 1;
   d.prefix_splits = p.prefix_splits;
+  // The prefix and suffix launches write disjoint split slots and meet only
+  // in the merge: the prefix goes on the side stream (high priority; the
+  // tcgen05 prefix grid is sized to about half the SMs) and the suffix on
+  // the caller's stream beside it, joined before the merge.
+  SideFork fork(dev, st);
+  if (int e = fork.begin()) return e;
+  const cudaStream_t pst = fork.stream();
   // prefix: every row against the shared keys, through sequence 0's table
   if (p.tc_prefix) {
     PrefillArgs f{};
@@ -791,13 +821,13 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
     if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
                                  cache->head_size, d.group))
       return e;
-    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, st));
+    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, pst));
   } else {
     DecodeArgs pa = d;
     pa.split_blocks = p.prefix_split_blocks;
     pa.prefix_len = p.prefix_blocks * kBlock;
     pa.prefix_col_groups = p.col_groups;
-    PKV_TRY(launch_cascade_prefix_bf16(kmap, vmap, pa, cache->head_size, st));
+    PKV_TRY(launch_cascade_prefix_bf16(kmap, vmap, pa, cache->head_size, pst));
   }
   // suffix: each row against its own keys after the prefix; then the merge
   DecodeArgs sa = d;
@@ -805,6 +835,7 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
   sa.key_begin_blocks = p.prefix_blocks;
   sa.split_base = p.prefix_splits;
   PKV_TRY(launch_decode_bf16(kmap, vmap, sa, cache->head_size, fp8, st));
+  if (int e = fork.join()) return e;
   PKV_TRY(launch_combine_bf16(sa, cache->head_size, st));
   return PKV_OK;
 }

@@ -19,12 +19,15 @@ def M(S, mcl, mq=1, w=0):
 
 
 @pytest.mark.parametrize("S,mcl,pblocks,want", [
-    (64, 3000, 128, True),      # 64 x 2048 shared keys (measured 1.4x)
-    (16, 9000, 512, True),      # 16 x 8192 (1.4x)
-    (256, 3000, 128, True),     # (2.0x)
-    (16, 3000, 128, False),     # 15 x 2048 < 64K: plain wins (0.99x)
-    (256, 1000, 32, False),     # prefix < 1024 tokens (1.02x)
-    (64, 1000, 32, False),      # (0.83x)
+    (64, 3000, 128, True),      # 64 x 2048 shared keys (measured 1.83x)
+    (16, 9000, 512, True),      # 16 x 8192 (1.62x)
+    (256, 3000, 128, True),     # (2.3x)
+    (16, 3000, 128, True),      # 15 x 2048 = 30K >= 16K (1.17x)
+    (8, 9000, 512, True),       # 7 x 8192 = 57K (1.19x)
+    (64, 1000, 32, True),       # 64 x 512: 63 x 512 = 32K (1.09x)
+    (16, 2000, 64, False),      # 15 x 1024 < 16K: plain wins (0.89x)
+    (8, 3000, 128, False),      # 7 x 2048 < 16K (0.89x)
+    (256, 1000, 16, False),     # prefix < 512 tokens (0.96x)
     (7, 90000, 4096, False),    # < 8 sequences: the pages' gate
     (64, 3000, 15, False),      # < 256 tokens: the pages' gate
     (64, 2048, 128, False),     # no key after the prefix

@@ -193,3 +193,33 @@ def test_forked_full_size_mixed_batch_matches_the_single_stream_order():
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert np.isfinite(out.float().cpu().numpy()).all()
+
+
+def test_cascade_forked_prefix_on_a_fresh_stream_is_ordered():
+    """Cascade: the shared-prefix launch goes on the side stream beside the
+    suffix launch; write + cascade + a copy of the output, back to back on a
+    new stream, three times, with no host synchronisation in between."""
+    rng = np.random.default_rng(7)
+    S, P = 24, 16
+    ctx = rng.integers(P * 16 + 1, P * 16 + 900, S, endpoint=True)
+    wl = W.make_workload([1] * S, ctx, num_q_heads=32, num_kv_heads=8, head_size=128, seed=7,
+                         shared_prefix_blocks=P, shared_seqs=tuple(range(S)))
+    exp, _, _, _ = oracle_step(wl)
+    g = wl.to("cuda")
+    meta = pkv.attn_meta(g.q, g.block_tables, g.context_lens, max_query_len=1,
+                         max_context_len=g.max_context_len)
+    ws = torch.empty(pkv.cascade_workspace_size(g.k_cache, meta, P), dtype=torch.uint8,
+                     device="cuda")
+    out = nan_like(g.q)
+    host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            out.fill_(float("nan"))
+            pkv.write(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache, stream=s)
+            pkv.attention_cascade(out, g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens,
+                                  g.query_start_loc, g.scale, P,
+                                  max_context_len=g.max_context_len, workspace=ws, stream=s)
+            host.copy_(out, non_blocking=True)
+    s.synchronize()
+    assert max_err(host, exp) <= TOL[torch.bfloat16]
