@@ -427,7 +427,10 @@ def run_pkv(args, rank, world, device):
     peak, peak_kind = hbm_peak()
     value = job_throughput(step_b, world, ms_per_step)
     achieved = attn_b / (attn_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name + ("-fp8" if fp8 else ""))
+    # the committed counters were taken on full-attention batches at the
+    # automatic split size: none for a window or a forced split
+    traffic = (recorded_traffic(wl.name + ("-fp8" if fp8 else ""))
+               if not args.window and not args.kv_split else None)
     line = {
         "metric": METRIC,
         "value": round(value, 1),

@@ -262,24 +262,27 @@ int check_meta(const pkv_cache_desc* c, const pkv_attn_meta* m) {
 // Cache blocks per decode split (CTA).  Measured on GB300 decode batches: 1024
 // keys (512 KB of K+V per kv head at D=128) by default; 2048 for long contexts
 // (>= 16K keys), which halves the split partials and the CTAs that find
-// nothing to do, as long as that still leaves four waves of CTAs; shorter
-// chunks only when the batch has too few (sequence, head) units to fill the
-// GPU twice over.  `max_blocks`: blocks the longest row reads; `units`:
-// (sequence, kv head, 8-head group) triples.
+// nothing to do; shorter chunks only while the batch would have fewer CTAs
+// than SMs.  A CTA's fixed costs (barriers, Q, the first TMA round trip, its
+// partial and the merge's read of it) outweigh more parallelism well before
+// the GPU is full twice over: 2 sequences x 8 kv heads x 32K keys run in 51 us
+// with 2048-key splits against 65 us with 512-key ones, 4 x 32 heads x 4K keys
+// in 46 against 49 us, 8 x 8 kv heads x 2K keys in 23 against 25 us.
+// `max_blocks`: blocks the longest row reads; `units`: (sequence, kv head,
+// 8-head group) triples.
 // Then the longest row's splits are evened out: their number is its blocks
 // over that size rounded to nearest rather than up, each ceil(blocks / n)
 // long and at most 128 (the kernel's 32 blocks per warp).  A 1024-key window
 // spans 65 blocks: one split of 65, not 64 + 1, which would also cost a
-// merge pass (measured on GB300 with 1024-key windows: 146 -> 141 us on the
+// merge pass (measured with 1024-key windows: 146 -> 141 us on the
 // 64 x 32-head batch, 112 -> 104 us on 256 x 8 kv heads, 27 -> 20 us on
 // 16 x 8 kv heads).
 int choose_split_blocks(int max_blocks, int64_t units, int num_sms, int kv_split_tokens) {
   if (kv_split_tokens > 0) return kv_split_tokens / kBlock;
-  const int64_t slots = 2LL * num_sms;  // two CTAs per SM
   auto ctas = [&](int sb) { return units * ((max_blocks + sb - 1) / sb); };
   int split_blocks = 64;
-  if (max_blocks * kBlock >= 16384 && ctas(128) >= 4 * slots) split_blocks = 128;
-  while (split_blocks > 4 && ctas(split_blocks) < 2 * slots) split_blocks /= 2;
+  if (max_blocks * kBlock >= 16384 && ctas(128) >= num_sms) split_blocks = 128;
+  while (split_blocks > 4 && ctas(split_blocks) < num_sms) split_blocks /= 2;
   if (max_blocks > 0) {
     constexpr int kMaxSplitBlocks = 128;
     int n = (max_blocks + split_blocks / 2) / split_blocks;
