@@ -79,10 +79,17 @@ def hbm_peak():
 
 
 def decode_source_hash() -> str:
+    """sha256 over what the decode kernel is compiled from: its source, the
+    common device header and its argument struct (DecodeArgs, the text of its
+    definition in pkv_internal.h; the other structs there do not reach it)."""
     h = hashlib.sha256()
-    for name in ("pkv_decode.cu", "pkv_common.cuh", "pkv_internal.h"):
+    for name in ("pkv_decode.cu", "pkv_common.cuh"):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(CSRC, "pkv_internal.h"), "rb") as f:
+        text = f.read()
+    a = text.index(b"struct DecodeArgs {")
+    h.update(text[a:text.index(b"};", a) + 2])
     return h.hexdigest()
 
 

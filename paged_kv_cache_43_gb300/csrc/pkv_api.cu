@@ -618,6 +618,7 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
     f.k_descale = k_descale;
     f.v_descale = v_descale;
     f.scale_log2 = scale * LOG2E;
+    f.longest_first = p.num_decode == 0 ? 1 : 0;   // alone on the GPU, or beside decode
     if (prefill_tc_supported(cache->head_size, G) && (!fp8 || cache->head_size == 128)) {
       // tcgen05/TMEM kernel: two tiles of 128/G tokens x G heads per CTA.
       const int toks = prefill_tc_tokens_per_cta(G);

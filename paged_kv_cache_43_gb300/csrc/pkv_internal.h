@@ -84,6 +84,10 @@ struct PrefillArgs {
   const float* k_descale;        // FP8 cache: [num_seqs_total, Hkv] (null otherwise)
   const float* v_descale;
   float scale_log2;
+  // tcgen05 kernel: hand the CTAs out longest first (a launch that has the
+  // GPU to itself); 0 keeps the plain order, whose short CTAs finish early
+  // and leave SMs to a decode launch running beside it.
+  int32_t longest_first;
   // Cascade prefix launch of the tcgen05 kernel (cascade_prefix = 1): the
   // decode rows 0 .. num_seqs - 1 (row t = sequence t) against the shared keys
   // [0, prefix_len) of block-table row 0, prefix_tiles 128-key tiles per CTA
