@@ -25,11 +25,12 @@ int g_num_sms[kMaxDevices] = {};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Per device: the stream a mixed batch's prefill launch runs on while its
-// decode launches run on the caller's stream, created once at the device's
-// greatest priority (so that the block scheduler hands freed SMs to the
-// prefill tiles first and the short decode CTAs fill the prefill's tail), and
-// the events that fork it from the caller's stream and join it back.  `mu`
+// Per device: the stream that a mixed batch's prefill launch (and a cascade
+// call's shared-prefix launch) runs on while the decode launches run on the
+// caller's stream, created once at the device's greatest priority (so that
+// the block scheduler hands freed SMs to the tensor-core tiles first and the
+// short decode CTAs fill their tail), and the events that fork it from the
+// caller's stream and join it back.  `mu`
 // keeps the record-wait-launch-record-wait sequence of one call from
 // interleaving with another thread's.  side == nullptr: not available (the
 // launches then stay on the caller's stream).
