@@ -32,6 +32,10 @@
 //    grows by more than 2^8), write P (bf16) to TMEM for the second MMA, and at
 //    the end read O, divide by the row sum and store bf16.  No shuffles: a
 //    thread holds its whole row.
+//  * a launch that has the GPU to itself hands its CTAs out longest first
+//    (each CTA ranks the (sequence, tile pair) units by the key tiles they
+//    see and takes the one whose rank is its launch index), so the last wave
+//    holds the short ones; beside a decode launch the plain order stays.
 //  * every wait is an mbarrier with a bounded spin and a CTA-wide abort flag;
 //    TMEM is freed on every path.
 //  * FP8 (e4m3) cache, head_size 128: TMA lands each tile's codes (128 keys x
