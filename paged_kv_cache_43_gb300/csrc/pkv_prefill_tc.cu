@@ -209,7 +209,7 @@ __device__ __forceinline__ int tc_unit_cost(const PrefillArgs& a, int u, int tok
 // Called by every thread of the CTA (it synchronises the CTA twice).
 __device__ __forceinline__ TcWork pick_work(const PrefillArgs& a, int toks, int32_t* scratch) {
   const int nu = a.num_seqs * a.num_mtiles;
-  if (!a.longest_first || nu > kLptUnits) {
+  if (nu > kLptUnits) {   // (the launcher does not choose this kernel then)
     return TcWork{a.seq_begin + static_cast<int>(blockIdx.z), static_cast<int>(blockIdx.y),
                   a.num_mtiles - 1 - static_cast<int>(blockIdx.x)};
   }
@@ -238,7 +238,9 @@ __device__ __forceinline__ TcWork pick_work(const PrefillArgs& a, int toks, int3
   return TcWork{a.seq_begin + u / a.num_mtiles, b % a.num_kv_heads, u % a.num_mtiles};
 }
 
-template <int D, bool FP8>
+// LPT: the longest-first instantiation (a separate kernel, so that the plain
+// one keeps its work indices as launch coordinates and its register budget).
+template <int D, bool FP8, bool LPT>
 __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
     pkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
@@ -264,15 +266,15 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
   const int tile_toks = kTcRows / G;                // tokens per query tile
   const int toks = kTcTiles * tile_toks;            // tokens per CTA
   int s, kvh, mtile;
-  if (casc) {
-    s = 0;
-    kvh = blockIdx.y;
-    mtile = a.num_mtiles - 1 - blockIdx.x;
-  } else {
+  if constexpr (LPT) {
     const TcWork w = pick_work(a, toks, reinterpret_cast<int32_t*>(sK));
     s = w.s;
     kvh = w.kvh;
     mtile = w.mtile;
+  } else {
+    s = casc ? 0 : a.seq_begin + blockIdx.z;
+    kvh = blockIdx.y;
+    mtile = a.num_mtiles - 1 - blockIdx.x;  // heaviest pair of each sequence first
   }
 
   const int L = casc ? a.prefix_len : __ldg(a.context_lens + s);
@@ -766,7 +768,9 @@ template <int D, bool FP8>
 cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                         const PrefillArgs& a, cudaStream_t stream) {
   constexpr int smem = tc_smem_bytes<D>();
-  auto kfn = pkv_prefill_tc_kernel<D, FP8>;
+  const bool lpt = a.longest_first && !a.cascade_prefix &&
+                   static_cast<int64_t>(a.num_seqs) * a.num_mtiles <= kLptUnits;
+  auto kfn = lpt ? pkv_prefill_tc_kernel<D, FP8, true> : pkv_prefill_tc_kernel<D, FP8, false>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // cascade prefix: grid.z = prefix key splits
