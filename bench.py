@@ -706,43 +706,54 @@ def pool_trace(pool, steps, running=256, prompt=768, shared=512, turnover=16, se
     interface): `running` requests whose prompts share a `shared`-token system
     prompt decode one token per step; every 16 steps `turnover` of them finish
     and as many new ones are admitted (prefix hits + prefill of the rest).
-    Returns (slots allocated, seconds)."""
+    The prompts are drawn before the clock starts (they are the trace's
+    input); the C++ pool gets numpy arrays, one batched call per decode step
+    for the appends and one for the slots, the oracle's pool Python lists and
+    one call per request.  Returns (slots allocated, seconds)."""
     rng = np.random.default_rng(seed)
-    system = [int(x) for x in rng.integers(0, 32000, shared)]
+    admissions = running + turnover * (steps // 16)
+    system = rng.integers(0, 32000, shared).astype(np.int32)
+    own = rng.integers(0, 32000, (admissions, prompt - shared)).astype(np.int32)
+    prompts = np.concatenate([np.broadcast_to(system, (admissions, shared)), own], axis=1)
     batched = hasattr(pool, "allocate_slots_batch")
+    if not batched:
+        prompts = prompts.tolist()
     live, next_id, slots = [], 0, 0
 
     def admit():
         nonlocal next_id, slots
         rid = next_id
         next_id += 1
-        toks = system + [int(x) for x in rng.integers(0, 32000, prompt - shared)]
+        toks = prompts[rid]
         pool.add_request(rid, toks)
         cached = pool.admit(rid)
-        s = pool.allocate_slots(rid, len(toks) - cached)
+        s = pool.allocate_slots(rid, prompt - cached)
         slots += len(s)
         live.append(rid)
 
     t0 = time.perf_counter()
     for _ in range(running):
         admit()
+    live_ids = np.asarray(live, dtype=np.int64)
+    ones = np.ones(running, dtype=np.int32)
+    step_tok = np.empty(running, dtype=np.int32)
     for step in range(steps):
         if batched:
-            pool.append_token_batch(live, [step] * len(live))
+            step_tok.fill(step)
+            pool.append_token_batch(live_ids, step_tok)
+            s, done = pool.allocate_slots_batch(live_ids, ones)
+            assert done == running
+            slots += len(s)
         else:
             for rid in live:
                 pool.append_token(rid, step)
-        if batched:
-            s, done = pool.allocate_slots_batch(live, [1] * len(live))
-            assert done == len(live)
-            slots += len(s)
-        else:
             for rid in live:
                 slots += len(pool.allocate_slots(rid, 1))
         if step % 16 == 15:
             for _ in range(turnover):
                 pool.free_request(live.pop(0))
                 admit()
+            live_ids = np.asarray(live, dtype=np.int64)
     return slots, time.perf_counter() - t0
 
 
