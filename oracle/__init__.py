@@ -254,24 +254,29 @@ def merge(ms, ls, accs):
 
 
 def cascade(problem: Problem, prefix_len: int):
-    """Cascade attention of a decode batch whose sequences share their first
+    """Cascade attention of a batch whose sequences share their first
     ``prefix_len`` keys ("Implémentation du cœur ... vLLM", ch. 6: the cascade
-    branch runs a prefix call and a suffix call and merges them with
-    merge_attn_states): per (sequence, q head) row, the state over the shared
+    branch runs a prefix call over every query token of the batch and a suffix
+    call over each sequence's own keys, and merges them with
+    merge_attn_states): per (query row, q head), the state over the shared
     keys [0, prefix_len) — the same physical blocks in every sequence's table,
-    the caller's contract — and the state over the row's own keys
-    [prefix_len, L), merged.  float64 [T, Hq, D]; decode rows only (one query
-    per sequence)."""
+    the caller's contract — and the state over the row's own visible keys
+    from prefix_len on (causal inside a chunk), merged.  float64 [T, Hq, D].
+    Every query row must sit after the prefix (position >= prefix_len): then
+    all shared keys are visible to it and the split is exact."""
     sh = problem.shape
     out = np.zeros((problem.num_tokens, sh["Hq"], sh["D"]), dtype=np.float64)
     for s in range(sh["S"]):
         q0 = int(problem.query_start_loc[s])
-        assert int(problem.query_start_loc[s + 1]) - q0 == 1
-        for hq in range(sh["Hq"]):
-            st0, m0, l0, a0 = row_state(problem, s, hq, 0, 0, prefix_len)
-            st1, m1, l1, a1 = row_state(problem, s, hq, 0, prefix_len)
-            assert st0 == 0 and st1 == 0
-            out[q0, hq] = merge([m0, m1], [l0, l1], [a0, a1])
+        qn = int(problem.query_start_loc[s + 1]) - q0
+        L = int(problem.context_lens[s])
+        assert L - qn >= prefix_len, "a query row inside the shared prefix"
+        for j in range(qn):
+            for hq in range(sh["Hq"]):
+                st0, m0, l0, a0 = row_state(problem, s, hq, j, 0, prefix_len)
+                st1, m1, l1, a1 = row_state(problem, s, hq, j, prefix_len)
+                assert st0 == 0 and st1 == 0
+                out[q0 + j, hq] = merge([m0, m1], [l0, l1], [a0, a1])
     return out
 
 

@@ -493,3 +493,33 @@ def test_cascade_decomposition_equals_attention(hq, hkv, pblocks):
                        A(wl.query_start_loc), wl.scale)
     got = oracle.cascade(P, pblocks * 16)
     np.testing.assert_allclose(got, exp, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("q_lens,pblocks", [([5, 1, 17, 3], 2), ([33, 16, 1], 4), ([1, 1, 40], 1)])
+def test_cascade_decomposition_equals_attention_for_chunks(q_lens, pblocks):
+    """The same with chunked-prefill rows (ch. 6: the prefix call covers every
+    query token of the batch): each chunk row's state over the shared keys
+    merged with its causal state over its own keys = its plain attention."""
+    S = len(q_lens)
+    rng = np.random.default_rng(sum(q_lens) + pblocks)
+    ctx = [pblocks * 16 + q + int(rng.integers(0, 60)) for q in q_lens]
+    wl = W.make_workload(q_lens, ctx, num_q_heads=8, num_kv_heads=2, head_size=64,
+                         dtype=torch.float32, seed=23 + pblocks, shared_prefix_blocks=pblocks,
+                         shared_seqs=tuple(range(S)))
+    exp, _, kc, vc = oracle_step(wl)
+    A = W.as_oracle_array
+    P = oracle.Problem(A(wl.q), kc, vc, A(wl.block_tables), A(wl.context_lens),
+                       A(wl.query_start_loc), wl.scale)
+    got = oracle.cascade(P, pblocks * 16)
+    np.testing.assert_allclose(got, exp, atol=1e-12, rtol=0)
+
+
+def test_cascade_refuses_a_row_inside_the_prefix():
+    wl = W.make_workload([4], [40], num_q_heads=2, num_kv_heads=2, head_size=64,
+                         dtype=torch.float32, seed=3)
+    exp, _, kc, vc = oracle_step(wl)
+    A = W.as_oracle_array
+    P = oracle.Problem(A(wl.q), kc, vc, A(wl.block_tables), A(wl.context_lens),
+                       A(wl.query_start_loc), wl.scale)
+    with pytest.raises(AssertionError):
+        oracle.cascade(P, 48)     # rows at positions 36..39 < 48
