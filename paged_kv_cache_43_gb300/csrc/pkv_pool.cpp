@@ -9,7 +9,10 @@
 //  * the free queue is an intrusive doubly linked list over block ids with a
 //    sentinel (index num_blocks), so a cache hit can unlink any block;
 //  * the prefix cache maps a 64-bit chained block hash to the blocks filed
-//    under it, oldest first (almost always one);
+//    under it, oldest first (almost always one): an open-addressing table
+//    (linear probing, backward-shift deletion, doubled when half full) whose
+//    entries hold the first and last block of a chain linked through
+//    per-block arrays, so filing and evicting a block allocate nothing;
 //  * a request keeps its token ids, its block ids and the hashes of its full
 //    blocks, extended incrementally as tokens become computed.
 #include <cstdint>
@@ -56,8 +59,59 @@ struct pkv_pool {
   std::vector<uint8_t> in_free, has_hash;
   std::vector<uint64_t> hash;
   int32_t num_free = 0, num_cached = 0;
-  std::unordered_map<uint64_t, std::vector<int32_t>> map;
+  // prefix cache: table entries (head < 0: empty) and the chains' links
+  struct Entry {
+    uint64_t key;
+    int32_t head, tail;
+  };
+  std::vector<Entry> table;
+  int shift = 0;           // index = (key * golden) >> shift; table.size() = 2^(64 - shift)
+  int64_t entries = 0;
+  std::vector<int32_t> hnext, hprev;
   std::unordered_map<int64_t, Request> reqs;
+
+  size_t home(uint64_t key) const {
+    return static_cast<size_t>((key * 0x9E3779B97F4A7C15ull) >> shift);
+  }
+  void init_table(int log2_size) {
+    shift = 64 - log2_size;
+    table.assign(size_t{1} << log2_size, Entry{0, -1, -1});
+  }
+  // Index of key's entry, or of the empty slot where it would go.
+  size_t probe(uint64_t key) const {
+    const size_t mask = table.size() - 1;
+    size_t i = home(key);
+    while (table[i].head >= 0 && table[i].key != key) i = (i + 1) & mask;
+    return i;
+  }
+  void grow() {
+    std::vector<Entry> old;
+    old.swap(table);
+    init_table(65 - shift);
+    for (const Entry& e : old)
+      if (e.head >= 0) table[probe(e.key)] = e;
+  }
+  void erase_entry(size_t i) {
+    const size_t mask = table.size() - 1;
+    size_t j = i;
+    while (true) {
+      j = (j + 1) & mask;
+      if (table[j].head < 0) break;
+      const size_t k = home(table[j].key);
+      // the entry at j may stay if its home lies cyclically in (i, j]
+      const bool stays = i <= j ? (i < k && k <= j) : (i < k || k <= j);
+      if (stays) continue;
+      table[i] = table[j];
+      i = j;
+    }
+    table[i].head = -1;
+    --entries;
+  }
+  // First block filed under key, or -1.
+  int32_t lookup(uint64_t key) const {
+    const Entry& e = table[probe(key)];
+    return e.head >= 0 ? e.head : -1;
+  }
 
   // ---- free queue
   void link_before(int32_t b, int32_t at) {  // insert b before `at`
@@ -86,14 +140,14 @@ struct pkv_pool {
   // ---- prefix cache
   void evict_hash(int32_t b) {
     if (!has_hash[b]) return;
-    auto it = map.find(hash[b]);
-    std::vector<int32_t>& v = it->second;
-    for (size_t i = 0; i < v.size(); ++i)
-      if (v[i] == b) {
-        v.erase(v.begin() + static_cast<std::ptrdiff_t>(i));
-        break;
-      }
-    if (v.empty()) map.erase(it);
+    const size_t i = probe(hash[b]);
+    Entry& e = table[i];
+    const int32_t p = hprev[b], n = hnext[b];
+    if (p >= 0) hnext[p] = n;
+    else e.head = n;
+    if (n >= 0) hprev[n] = p;
+    else e.tail = p;
+    if (e.head < 0) erase_entry(i);
     has_hash[b] = 0;
     --num_cached;
   }
@@ -102,7 +156,21 @@ struct pkv_pool {
     evict_hash(b);
     hash[b] = h;
     has_hash[b] = 1;
-    map[h].push_back(b);
+    hnext[b] = -1;
+    size_t i = probe(h);
+    if (table[i].head >= 0) {  // append to the chain: lookups return the oldest
+      hprev[b] = table[i].tail;
+      hnext[table[i].tail] = b;
+      table[i].tail = b;
+    } else {
+      if (2 * (entries + 1) > static_cast<int64_t>(table.size())) {
+        grow();
+        i = probe(h);
+      }
+      hprev[b] = -1;
+      table[i] = Entry{h, b, b};
+      ++entries;
+    }
     ++num_cached;
   }
 
@@ -151,6 +219,9 @@ pkv_pool* pkv_pool_create(int32_t num_blocks, int32_t block_size, int32_t enable
     p->in_free.assign(num_blocks, 0);
     p->has_hash.assign(num_blocks, 0);
     p->hash.assign(num_blocks, 0);
+    p->hnext.assign(num_blocks, -1);
+    p->hprev.assign(num_blocks, -1);
+    p->init_table(10);
   } catch (...) {
     delete p;
     return nullptr;
@@ -210,9 +281,9 @@ int pkv_pool_admit(pkv_pool* pool, int64_t req_id, int32_t* num_cached_tokens) {
   const int32_t cap = (static_cast<int32_t>(r.tokens.size()) - 1) / pool->bs;
   pool->extend_hashes(r, cap);
   for (int32_t i = 0; i < cap; ++i) {
-    auto m = pool->map.find(r.hashes[i]);
-    if (m == pool->map.end()) break;
-    r.blocks.push_back(m->second.front());
+    const int32_t b = pool->lookup(r.hashes[i]);
+    if (b < 0) break;
+    r.blocks.push_back(b);
   }
   for (int32_t b : r.blocks) pool->touch(b);
   r.num_computed = static_cast<int32_t>(r.blocks.size()) * pool->bs;

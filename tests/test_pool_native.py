@@ -27,19 +27,21 @@ def _same_state(o, n, live, nb):
         assert n.num_computed(rid) == o.num_computed(rid)
 
 
-def _trace(seed, nb, caching, window, steps=400):
+def _trace(seed, nb, caching, window, steps=400, vocab=50, max_prompt=80, max_own=40,
+           check_every=1):
     rng = random.Random(seed)
     o, n = O.Pool(nb, caching=caching), N.BlockPool(nb, caching=caching)
     assert n.null_block == o.null_block
-    prompts = [[rng.randrange(50) for _ in range(rng.randrange(16, 80))] for _ in range(3)]
+    prompts = [[rng.randrange(vocab) for _ in range(rng.randrange(16, max_prompt))]
+               for _ in range(3)]
     live, next_id = [], 0
-    for _ in range(steps):
+    for step in range(steps):
         op = rng.random()
         if op < 0.25 or not live:
             rid = next_id
             next_id += 1
             base = rng.choice(prompts) if rng.random() < 0.7 else []
-            toks = base + [rng.randrange(50) for _ in range(rng.randrange(1, 40))]
+            toks = base + [rng.randrange(vocab) for _ in range(rng.randrange(1, max_own))]
             o.add_request(rid, toks)
             n.add_request(rid, toks)
             assert n.admit(rid) == o.admit(rid)
@@ -59,7 +61,7 @@ def _trace(seed, nb, caching, window, steps=400):
             rid = rng.choice(live)
             todo = len(o.reqs[rid].tokens) - o.num_computed(rid)
             if todo <= 0:
-                t = rng.randrange(50)
+                t = rng.randrange(vocab)
                 o.append_token(rid, t)
                 n.append_token(rid, t)
                 todo = 1
@@ -76,7 +78,9 @@ def _trace(seed, nb, caching, window, steps=400):
             rid = live.pop(rng.randrange(len(live)))
             o.free_request(rid)
             n.free_request(rid)
-        _same_state(o, n, live, nb)
+        if step % check_every == check_every - 1:
+            _same_state(o, n, live, nb)
+    _same_state(o, n, live, nb)
     n.close()
 
 
@@ -85,6 +89,16 @@ def _trace(seed, nb, caching, window, steps=400):
                                                 (40, True, 40), (40, True, 17), (16, False, 9)])
 def test_native_pool_matches_oracle_on_random_traces(seed, nb, caching, window):
     _trace(seed * 131 + nb, nb, caching, window)
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_native_pool_matches_oracle_with_thousands_of_cached_blocks(seed):
+    """A pool of 3000 blocks with a large vocabulary: the prefix table grows
+    several times and most evictions remove an entry (backward-shift
+    deletion under collisions); the full state is compared every 50
+    operations and at the end."""
+    _trace(seed + 77, 3000, True, 0, steps=1500, vocab=32000, max_prompt=400, max_own=300,
+           check_every=50)
 
 
 def test_block_tables_rows_and_errors():
