@@ -4,9 +4,11 @@ The loop is the consumer the pages describe for the pool ("Kh√°m ph√° vLLM: Gi·∫
 ph·∫´u h·ªá th·ªëng suy lu·∫≠n LLM th√¥ng l∆∞·ª£ng cao", "allocate_slots" and "Ch·∫°y
 forward pass"; "Impl√©mentation du c≈ìur du moteur d'inf√©rence haute
 performance vLLM" ch. 4 ¬ß4.3 on allocation and recompute preemption): each
-step gives every running request one decode token, admits waiting requests
-(prefix-cache hits first, then their remaining prompt as one chunk) while the
-token budget and the pool allow, preempts the most recently admitted request
+step gives every decoding request one token, every request still in its
+prompt its next chunk, and admits waiting requests (prefix-cache hits first,
+then the first chunk of their remaining prompt) while the token budget and
+the pool allow -- a prompt longer than the budget is prefilled in chunks over
+several steps -- preempts the most recently admitted request
 when a decode finds no block (its blocks go back; it is re-admitted later and
 recomputes what the cache no longer holds), writes the step's K/V rows with
 pkv_write at the pool's slots and runs pkv_attention over the pool's block
@@ -116,16 +118,24 @@ class DecodeLoop:
         sched = []        # (req, positions, slots)
         preempted = []
         budget = self.max_batch_tokens
-        # running requests: one decode token each (the last sampled token)
-        for r in sorted(self.running, key=lambda x: x.admitted_order):
+        # running requests, oldest first: a decoding request computes its last
+        # sampled token; one still in its prompt computes its next chunk, as
+        # much of the rest as the token budget leaves (decodes go first)
+        order = sorted(self.running, key=lambda x: (self.pool.num_computed(x.rid) + 1 <
+                                                    len(x.tokens), x.admitted_order))
+        for r in order:
             if r not in self.running:
                 continue
             while True:
                 pos = self.pool.num_computed(r.rid)
-                slots = self.pool.allocate_slots(r.rid, 1, self.window)
+                rest = len(r.tokens) - pos
+                n = 1 if rest <= 1 else min(rest, budget)
+                if n <= 0:
+                    break                        # no budget left for its next chunk
+                slots = self.pool.allocate_slots(r.rid, n, self.window)
                 if slots is not None:
-                    sched.append((r, [pos], slots))
-                    budget -= 1
+                    sched.append((r, list(range(pos, pos + n)), slots))
+                    budget -= n
                     break
                 victim = max(self.running, key=lambda x: x.admitted_order)
                 self._preempt(victim)
@@ -133,15 +143,13 @@ class DecodeLoop:
                 sched = [s for s in sched if s[0] is not victim]
                 if victim is r:
                     break
-        # waiting requests: prefix hits, then the rest of their known tokens
+        # waiting requests: prefix hits, then the first chunk of the rest of
+        # their known tokens (chunked prefill: at most the budget left)
         while self.waiting and budget > 0:
             r = self.waiting[0]
             self.pool.add_request(r.rid, r.tokens)
             cached = self.pool.admit(r.rid)
-            n = len(r.tokens) - cached
-            if n > budget:
-                self.pool.free_request(r.rid)
-                break
+            n = min(len(r.tokens) - cached, budget)
             first = cached
             slots = self.pool.allocate_slots(r.rid, n, self.window)
             if slots is None:
@@ -202,7 +210,7 @@ class DecodeLoop:
         finished = []
         for r, positions, _ in sched:
             if positions[-1] + 1 < len(r.tokens):
-                continue                  # (chunk did not reach the end: not the case here)
+                continue                  # a prompt chunk short of the end: nothing to sample
             rng = np.random.default_rng((self.seed, r.rid, r.generated))
             r.tokens.append(int(rng.integers(self.vocab)))
             self.pool.append_token(r.rid, r.tokens[-1])

@@ -68,3 +68,45 @@ def test_host_loop_invariants(_stub_kernels, num_blocks, caching, window):
     if num_blocks == 14:
         assert preempted > 0
     assert loop.pool.num_free() == num_blocks - 1             # everything returned
+
+
+@pytest.mark.parametrize("caching", [True, False])
+def test_host_loop_prefills_long_prompts_in_chunks(_stub_kernels, caching):
+    """Prompts longer than the token budget are prefilled over several steps:
+    every chunk fits the budget left after that step's decode rows, a
+    request's chunks cover its prompt positions once and in order, it samples
+    nothing before its prompt is done, and everything finishes."""
+    rng = np.random.default_rng(11)
+    budget = 48
+    loop = DL.DecodeLoop(num_blocks=200, num_q_heads=4, num_kv_heads=2, head_size=64,
+                         caching=caching, max_batch_tokens=budget, device="cpu")
+    system = [int(x) for x in rng.integers(0, 512, 70)]
+    want, prompt_len = {}, {}
+    for i in range(6):
+        p = system + [int(x) for x in rng.integers(0, 512, int(rng.integers(10, 90)))]
+        n = int(rng.integers(3, 12))
+        rid = loop.add_request(p, n)
+        want[rid], prompt_len[rid] = len(p) + n, len(p)
+    covered = {rid: [] for rid in want}
+    chunked = set()
+    done, steps = set(), 0
+    while not loop.done():
+        st = loop.step()
+        assert st is not None
+        steps += 1
+        nd = sum(1 for x in st.q_lens if x == 1)
+        assert sum(st.q_lens) <= max(budget, nd)      # decode rows are never held back
+        for i, rid in enumerate(st.req_ids):
+            pos = st.positions[i]
+            assert pos == list(range(pos[0], pos[0] + len(pos)))
+            if pos[-1] + 1 < prompt_len[rid]:
+                chunked.add(rid)
+                assert rid not in st.finished
+            covered[rid].extend(pos)
+        done |= set(st.finished)
+        assert steps < 2000
+    assert done == set(want)
+    assert chunked                               # some prompt did take several steps
+    for rid, pos in covered.items():
+        assert max(pos) == want[rid] - 2         # the last sampled token is never computed
+    assert loop.pool.num_free() == 200 - 1
