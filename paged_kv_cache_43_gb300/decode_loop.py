@@ -129,9 +129,9 @@ class DecodeLoop:
             while True:
                 pos = self.pool.num_computed(r.rid)
                 rest = len(r.tokens) - pos
-                n = 1 if rest <= 1 else min(rest, budget)
+                n = min(1 if rest <= 1 else rest, budget)
                 if n <= 0:
-                    break                        # no budget left for its next chunk
+                    break                        # no budget left for its next row(s)
                 slots = self.pool.allocate_slots(r.rid, n, self.window)
                 if slots is not None:
                     sched.append((r, list(range(pos, pos + n)), slots))
@@ -140,6 +140,7 @@ class DecodeLoop:
                 victim = max(self.running, key=lambda x: x.admitted_order)
                 self._preempt(victim)
                 preempted.append(victim.rid)
+                budget += sum(len(s[1]) for s in sched if s[0] is victim)   # its rows go back
                 sched = [s for s in sched if s[0] is not victim]
                 if victim is r:
                     break

@@ -94,8 +94,7 @@ def test_host_loop_prefills_long_prompts_in_chunks(_stub_kernels, caching):
         st = loop.step()
         assert st is not None
         steps += 1
-        nd = sum(1 for x in st.q_lens if x == 1)
-        assert sum(st.q_lens) <= max(budget, nd)      # decode rows are never held back
+        assert sum(st.q_lens) <= budget              # the token budget holds every step
         for i, rid in enumerate(st.req_ids):
             pos = st.positions[i]
             assert pos == list(range(pos[0], pos[0] + len(pos)))
@@ -110,3 +109,21 @@ def test_host_loop_prefills_long_prompts_in_chunks(_stub_kernels, caching):
     for rid, pos in covered.items():
         assert max(pos) == want[rid] - 2         # the last sampled token is never computed
     assert loop.pool.num_free() == 200 - 1
+
+
+def test_more_decodes_than_the_budget_wait_their_turn():
+    """With more running decodes than the token budget, a step takes only as
+    many rows as the budget allows (oldest first); the rest wait, and all
+    finish."""
+    loop = DL.DecodeLoop(num_blocks=200, num_q_heads=4, num_kv_heads=2, head_size=64,
+                         caching=False, max_batch_tokens=4, device="cpu")
+    rng = np.random.default_rng(5)
+    rids = [loop.add_request([int(x) for x in rng.integers(0, 512, 3)], 6) for _ in range(7)]
+    done, steps = set(), 0
+    while not loop.done():
+        st = loop.step()
+        assert st is not None and 0 < sum(st.q_lens) <= 4
+        done |= set(st.finished)
+        steps += 1
+        assert steps < 500
+    assert done == set(rids)

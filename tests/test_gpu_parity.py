@@ -282,19 +282,16 @@ def test_full_size_step_sampled_against_oracle(n):
         assert not st.any()
         err = max_err(out[torch.as_tensor(rows, device="cuda")], exp)
         assert err <= 2e-2, err
-    pf = list(range(nd, g.num_seqs))[:2]
+    # every row and head of every prefill chunk (the tcgen05 kernel's tile
+    # pairs, row tails and key tails all live in these 512-row chunks)
+    pf = list(range(nd, g.num_seqs))
     if pf:
         P, rows = compact_subproblem(g, pf, pre_k, pre_v)
-        got = as_f64(out)[rows]
-        errs = []
-        for i in range(len(pf)):
-            q0, n_q = int(P.query_start_loc[i]), int(P.query_start_loc[i + 1] - P.query_start_loc[i])
-            for j in sorted({0, 1, n_q // 2, n_q - 1}):
-                for h in range(g.num_q_heads):
-                    st, m, l, acc = oracle.row_state(P, i, h, j)
-                    assert st == 0
-                    errs.append(np.abs(got[q0 + j, h] - acc / l).max())
-        assert max(errs) <= 2e-2, max(errs)
+        exp, st = oracle.attention(P.q, P.k_cache, P.v_cache, P.block_tables,
+                                   P.context_lens, P.query_start_loc, g.scale)
+        assert not st.any()
+        err = max_err(out[torch.as_tensor(rows, device="cuda")], exp)
+        assert err <= 2e-2, err
 
 
 # ------------------------------------------------------------ CUDA graphs
