@@ -58,12 +58,34 @@ namespace {
 constexpr int kTcRows = 128;      // UMMA M (rows of one query tile)
 constexpr int kTcTiles = 2;       // query tiles per CTA
 constexpr int kTcKeys = 128;      // keys per K/V tile
-constexpr int kTcThreads = 320;   // load, MMA, 2 x 4 softmax warps
-constexpr int kTcThreadsFp8 = 384;  // + two warps widening e4m3 K and V tiles
-// (12 warps put 3 on each SM sub-partition, the same register cap per thread
-// as 10: the 64K-entry file split four ways, 16K / (3 x 32) = 170.)
-constexpr int kKStages = 3;       // K ring depth
-constexpr int kVStages = 2;       // V ring depth
+// Warps: 0-3 softmax of query tile 0, 4-7 of query tile 1 (warpgroups 0 and
+// 1: warp w reads TMEM lanes 32 (w % 4) ..), 8 the TMA producer, 9 the MMA
+// issuer, 10-11 widen e4m3 K and V tiles (FP8 cache; idle otherwise).  The
+// launch gives each thread 168 registers; warpgroup 2 then hands registers
+// back so that the softmax warpgroups run at 208 (2 x 128 x 208 + 128 x 80 =
+// 384 x 168).
+constexpr int kTcThreads = 384;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 80;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kTcThreads * 168, "register split");
+// Of every 8 packed pairs of scores, this many are exponentiated by the
+// polynomial on the FMA pipe and the rest by the MUFU.
+#ifndef PKV_TC_EMU_PAIRS
+#define PKV_TC_EMU_PAIRS 0
+#endif
+constexpr int kEmuPairs = PKV_TC_EMU_PAIRS;
+// bf16: one MMA-issuing thread per query tile (1) or one for both (0).
+#ifndef PKV_TC_TWO_ISSUERS
+#define PKV_TC_TWO_ISSUERS 0
+#endif
+#ifndef PKV_TC_KSTAGES
+#define PKV_TC_KSTAGES 3
+#endif
+#ifndef PKV_TC_VSTAGES
+#define PKV_TC_VSTAGES 2
+#endif
+constexpr int kKStages = PKV_TC_KSTAGES;   // K ring depth
+constexpr int kVStages = PKV_TC_VSTAGES;   // V ring depth
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S of tile t at 128t (P of tile t over its first 64 columns),
 // O of tile t at 256 + 128t.
@@ -99,15 +121,40 @@ constexpr int tc_smem_bytes() {
   return need > 120 * 1024 ? need : 120 * 1024;
 }
 
+// Timeline of one CTA (profiling builds, -DPKV_TC_TIMELINE): %globaltimer
+// stamps of the pipeline events of the CTA computing the last row-tile pair
+// of the batch's second sequence, kv head 0.
+#ifdef PKV_TC_TIMELINE
+__device__ unsigned long long g_tc_timeline[4096];
+#define TC_MARK(idx)                                         \
+  do {                                                       \
+    if (tl_on) g_tc_timeline[(idx)] = global_timer_ns();     \
+  } while (0)
+#else
+#define TC_MARK(idx) \
+  do {               \
+  } while (0)
+#endif
+
+__device__ __forceinline__ void set_max_regs_inc_softmax() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+}
+__device__ __forceinline__ void set_max_regs_dec_other() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+}
+
 // Bounded wait that also gives up when another thread of the CTA has aborted.
+// mbarrier.try_wait suspends the thread in hardware until the phase completes
+// or a short time limit passes, so a waiting warp takes no issue slots from
+// the softmax and MMA-issuing warps of its SM sub-partition.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int32_t* abort, int32_t* err) {
-  if (mbar_test(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_test(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
@@ -125,7 +172,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   bool ok = true;
   if (lane == 0) ok = wait_or_abort(bar, parity, abort, err);
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  if (ok && lane != 0) ok = wait_or_abort(bar, parity, abort, err);
+  if (ok && lane != 0) ok = mbar_test(bar, parity);   // completed: observe it
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -241,7 +288,7 @@ __device__ __forceinline__ TcWork pick_work(const PrefillArgs& a, int toks, int3
 // LPT: the longest-first instantiation (a separate kernel, so that the plain
 // one keeps its work indices as launch coordinates and its register budget).
 template <int D, bool FP8, bool LPT>
-__global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     pkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -277,6 +324,9 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
     mtile = a.num_mtiles - 1 - blockIdx.x;  // heaviest pair of each sequence first
   }
 
+#ifdef PKV_TC_TIMELINE
+  const bool tl_on = !casc && s == a.seq_begin + 1 && kvh == 0 && mtile == a.num_mtiles - 1;
+#endif
   const int L = casc ? a.prefix_len : __ldg(a.context_lens + s);
   const int q0 = casc ? 0 : __ldg(a.query_start_loc + s);
   const int qn = casc ? a.num_seqs : __ldg(a.query_start_loc + s + 1) - q0;
@@ -335,7 +385,10 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
     prefetch_tensor_map(&kmap);
     prefetch_tensor_map(&vmap);
     mbar_init(q_full, 1);
-    mbar_init(drain, 1);
+    // bf16: one MMA-issuing thread per query tile, each committing its own
+    // products (FP8: one thread issues both tiles' products)
+    const uint32_t issuers = (FP8 || !PKV_TC_TWO_ISSUERS) ? 1u : static_cast<uint32_t>(ntq);
+    mbar_init(drain, issuers);
     mbar_init(smem_u32(&sh->q_conv), 8);   // one arrival per softmax warp
     for (int t = 0; t < kTcTiles; ++t) {
       mbar_init(smem_u32(&sh->s_full[t]), 1);
@@ -344,29 +397,36 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
     }
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(smem_u32(&sh->k_full[i]), 1);
-      mbar_init(smem_u32(&sh->k_empty[i]), 1);
+      mbar_init(smem_u32(&sh->k_empty[i]), issuers);
       mbar_init(smem_u32(&sh->k_land[i]), 1);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(smem_u32(&sh->v_full[i]), 1);
-      mbar_init(smem_u32(&sh->v_empty[i]), 1);
+      mbar_init(smem_u32(&sh->v_empty[i]), issuers);
       mbar_init(smem_u32(&sh->v_land[i]), 1);
     }
     sh->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tc::alloc(smem_u32(&sh->tmem_base), kTmemCols);
+  if (warp == 9) tc::alloc(smem_u32(&sh->tmem_base), kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
   volatile int32_t* abort = &sh->abort;
+  TC_MARK(0);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp >= 8) {
+   set_max_regs_dec_other();
+   if (warp == 8 || (!FP8 && warp == 10)) {
+    // ------------------------------------------------------------ producers
+    // bf16: warp 8 streams the K tiles and warp 10 the V tiles, each through
+    // its own ring, so that neither waits behind the other's ring.  FP8:
+    // warp 8 streams both (K of tile it before V of tile it - 1); warps 10
+    // and 11 widen them.
     const uint64_t keep = policy_evict_normal();   // K/V tiles are re-read by the
     const int32_t* bt = a.block_tables + static_cast<int64_t>(s) * a.bt_stride;  // other row tiles
-    if (lane == 0) {
+    if (warp == 8 && lane == 0) {
       mbar_arrive_expect_tx(q_full, ntq * Lt::kQTile);
       for (int t = 0; t < ntq; ++t)
 #pragma unroll
@@ -374,21 +434,24 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
           tma_load_3d(smem_u32(sQ + t * Lt::kQTile + h * Lt::kQHalf), &qmap, q_full, h * 64,
                       kvh * G, q0 + tok0 + t * tile_toks, keep);
     }
-    // Lanes 0..7 hold the block ids of one tile (ids of tile it + 1 are loaded
-    // while tile it is issued).  K of tile it goes out before V of tile it - 1.
     constexpr int kBlocks = kTcKeys / kBlock;      // cache blocks per tile
-    auto load_ids = [&](int it) {
-      const int b = it * kBlocks + lane;
-      return (lane < kBlocks && it < ntiles && b < nblk) ? __ldg(bt + b) : -1;
+    // Block ids of four consecutive tiles per warp-wide load: lane l holds
+    // block l % 8 of ring position 4g + l / 8.  Group g + 1 is loaded while
+    // group g is issued, so no tile waits on its ids.
+    auto load_ids4 = [&](int g) {
+      const int it = j0 + 4 * g + (lane >> 3);
+      const int b = it * kBlocks + (lane & 7);
+      return (it < ntiles && b < nblk) ? __ldg(bt + b) : -1;
     };
-    // Issues the K (is_v = false) or V tile `it` into `dst`, completing on `full`.
-    auto issue_tile = [&](int it, int ids, bool is_v, uint32_t dst, uint32_t full) {
+    // Issues the K (is_v = false) or V tile `it` into `dst`, completing on
+    // `full`; its ids are lanes 8 sub .. 8 sub + 7 of `ids`.
+    auto issue_tile = [&](int it, int ids, int sub, bool is_v, uint32_t dst, uint32_t full) {
       bool ok[kBlocks];
       int bid[kBlocks];
       uint32_t bytes = 0;
 #pragma unroll
       for (int b = 0; b < kBlocks; ++b) {
-        bid[b] = __shfl_sync(0xffffffffu, ids, b);
+        bid[b] = __shfl_sync(0xffffffffu, ids, 8 * sub + b);
         const int blk = it * kBlocks + b;
         const bool in_range = blk < nblk && blk >= b_lo;
         ok[b] = in_range && bid[b] >= 0 && bid[b] < a.num_blocks;
@@ -416,132 +479,202 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
         }
       }
     };
-    int ids_cur = load_ids(j0), ids_prev = -1;
-    for (int it = j0; it <= ntiles; ++it) {
-      const int ids_next = load_ids(it + 1);
-      if (it < ntiles) {
-        const int rel = it - j0;  // ring position of K tile `it`
-        const int st = rel % kKStages;
-        if (rel >= kKStages &&
-            !warp_wait(smem_u32(&sh->k_empty[st]), ((rel / kKStages) - 1) & 1, abort, a.err))
+    int g_prev = -1, g_cur = load_ids4(0), g_nxt = load_ids4(1);
+    if constexpr (!FP8) {
+      const bool is_v = warp == 10;
+      const int stages = is_v ? kVStages : kKStages;
+      for (int rel = 0; rel < n_rel; ++rel) {
+        if (rel > 0 && (rel & 3) == 0) {
+          g_cur = g_nxt;
+          g_nxt = load_ids4((rel >> 2) + 1);
+        }
+        const int st = rel % stages;
+        if (rel >= stages &&
+            !warp_wait(smem_u32(is_v ? &sh->v_empty[st] : &sh->k_empty[st]),
+                       ((rel / stages) - 1) & 1, abort, a.err))
           break;
-        // (FP8: the codes land on k_land; warp 10 widens them, then k_full)
-        issue_tile(it, ids_cur, false, smem_u32(sK + st * Lt::kTileBytes),
-                   smem_u32(FP8 ? &sh->k_land[st] : &sh->k_full[st]));
+        issue_tile(j0 + rel, g_cur, rel & 3, is_v,
+                   smem_u32((is_v ? sV : sK) + st * Lt::kTileBytes),
+                   smem_u32(is_v ? &sh->v_full[st] : &sh->k_full[st]));
+        if (lane == 0) TC_MARK((is_v ? 200 : 100) + (rel & 63));
       }
-      if (it >= j0 + 1) {
-        const int iv = it - 1;
-        const int rv = iv - j0;   // ring position of V tile `iv`
-        const int st = rv % kVStages;
-        if (rv >= kVStages &&
-            !warp_wait(smem_u32(&sh->v_empty[st]), ((rv / kVStages) - 1) & 1, abort, a.err))
-          break;
-        issue_tile(iv, ids_prev, true, smem_u32(sV + st * Lt::kTileBytes),
-                   smem_u32(FP8 ? &sh->v_land[st] : &sh->v_full[st]));
+    } else {
+      for (int rel = 0; rel <= n_rel; ++rel) {
+        if (rel > 0 && (rel & 3) == 0) {
+          g_prev = g_cur;
+          g_cur = g_nxt;
+          g_nxt = load_ids4((rel >> 2) + 1);
+        }
+        if (rel < n_rel) {
+          const int st = rel % kKStages;
+          if (rel >= kKStages &&
+              !warp_wait(smem_u32(&sh->k_empty[st]), ((rel / kKStages) - 1) & 1, abort, a.err))
+            break;
+          // (the codes land on k_land; warp 10 widens them, then k_full)
+          issue_tile(j0 + rel, g_cur, rel & 3, false, smem_u32(sK + st * Lt::kTileBytes),
+                     smem_u32(&sh->k_land[st]));
+          if (lane == 0) TC_MARK(100 + (rel & 63));
+        }
+        if (rel >= 1) {
+          const int rv = rel - 1;   // ring position of the V tile
+          const int st = rv % kVStages;
+          if (rv >= kVStages &&
+              !warp_wait(smem_u32(&sh->v_empty[st]), ((rv / kVStages) - 1) & 1, abort, a.err))
+            break;
+          issue_tile(j0 + rv, (rv >> 2) == (rel >> 2) ? g_cur : g_prev, rv & 3, true,
+                     smem_u32(sV + st * Lt::kTileBytes), smem_u32(&sh->v_land[st]));
+          if (lane == 0) TC_MARK(200 + (rv & 63));
+        }
       }
-      ids_prev = ids_cur;
-      ids_cur = ids_next;
     }
-  } else if (warp == 1) {
+   } else if (warp == 9 || (!FP8 && PKV_TC_TWO_ISSUERS && warp == 11)) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t idS = FP8 ? tc::idesc_f16_f32(kTcRows, kTcKeys, 0, 0)
                                    : tc::idesc_bf16_f32(kTcRows, kTcKeys, 0, 0);
       constexpr uint32_t idO = FP8 ? tc::idesc_f16_f32(kTcRows, D, 0, 1)
                                    : tc::idesc_bf16_f32(kTcRows, D, 0, 1);
+      // Shared-memory descriptors are built once: the address field is the
+      // low 14 bits (address / 16) and never carries, so an operand at a
+      // constant byte offset is the base descriptor plus offset / 16 -- one
+      // add per MMA on the issuing thread, whose instructions compete with
+      // the softmax warps for the same issue slots.
+      const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(sV), Lt::kKvHalf, 1024);
       auto issue_s = [&](int t, int j) {
-        const uint32_t q_addr = smem_u32(sQ + t * Lt::kQTile);
-        const uint32_t k_addr = smem_u32(sK + (j % kKStages) * Lt::kTileBytes);
+        const uint64_t da0 = dq0 + static_cast<uint64_t>((t * Lt::kQTile) >> 4);
+        const uint64_t db0 = dk0 + static_cast<uint64_t>(((j % kKStages) * Lt::kTileBytes) >> 4);
+        const uint32_t d = tmem + col_s(t);
+        // K-step k: 16 bf16 = 32 B along the swizzled 128-B row, 64 columns
+        // per half (16 KB apart for both operands)
+        static_assert(Lt::kQHalf == Lt::kKvHalf, "equal half strides");
+        if constexpr (D == 128) {
+          tc::mma_ss_x8<2, 4, 6, 1024, 1026, 1028, 1030, 2, 4, 6, 1024, 1026, 1028, 1030>(
+              d, da0, db0, idS, 0u);
+        } else {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;  // 16 bf16 = 32 B along the swizzled row
-          const uint64_t da =
-              tc::smem_desc_sw128(q_addr + (kk >> 2) * Lt::kQHalf + off, 16, 1024);
-          const uint64_t db =
-              tc::smem_desc_sw128(k_addr + (kk >> 2) * Lt::kKvHalf + off, 16, 1024);
-          tc::mma_ss(tmem + col_s(t), da, db, idS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::mma_ss(d, da0 + (kk * 32 >> 4), db0 + (kk * 32 >> 4), idS, kk > 0 ? 1u : 0u);
         }
         tc::commit(smem_u32(&sh->s_full[t]));
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t v_addr = smem_u32(sV + (j % kVStages) * Lt::kTileBytes);
-#pragma unroll
-        for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-          const uint64_t dv = tc::smem_desc_sw128(v_addr + ks * 2048, Lt::kKvHalf, 1024);
-          tc::mma_ts(tmem + col_o(t), tmem + col_p(t) + ks * 8, dv, idO,
-                     (j > 0 || ks > 0) ? 1u : 0u);
-        }
+        const uint64_t db0 = dv0 + static_cast<uint64_t>(((j % kVStages) * Lt::kTileBytes) >> 4);
+        tc::mma_ts_x8(tmem + col_o(t), tmem + col_p(t), db0, idO, j > 0 ? 1u : 0u);
         tc::commit(smem_u32(&sh->pv_done[t]));
       };
-      // Event loop: issue whichever MMA is ready, never blocking on one
-      // query tile while the other could use the tensor core.  No barrier
-      // phase can run more than one ahead of what this thread has seen, so
-      // parity probes are unambiguous.
-      int s_next[kTcTiles] = {0, 0};   // next tile index whose S is issued
-      int pv_next[kTcTiles] = {0, 0};  // next tile index whose P V is issued
-      int k_released = 0, v_released = 0;  // ring stages handed back to the producer
-      bool ok = wait_or_abort(q_ready, 0, abort, a.err);
-      uint64_t idle_since = 0;
-      while (ok) {
-        bool progress = false;
-        for (int t = 0; t < ntq; ++t) {
-          const int jp = pv_next[t];
-          if (jp < s_next[t] && mbar_test(smem_u32(&sh->p_full[t]), jp & 1) &&
-              mbar_test(smem_u32(&sh->v_full[jp % kVStages]), (jp / kVStages) & 1)) {
+      if constexpr (!FP8 && PKV_TC_TWO_ISSUERS) {
+        // One issuing thread per query tile (warp 9: tile 0, warp 11: tile
+        // 1), on different SM sub-partitions: a single issuer shares its
+        // sub-partition's issue slots with two busy softmax warps and is
+        // starved by them (measured on GB300: an issuing thread beside one
+        // FMA-bound warp gets an MMA out every ~240 cycles instead of 64).
+        // Per tile the order is S(0), P(0) V, S(1), P(1) V, ...: S(j + 1)
+        // overwrites the columns P(j) lives in, and one thread's MMAs execute
+        // in issue order.
+        const int t = warp == 9 ? 0 : 1;
+        if (t < ntq) {
+          bool ok = wait_or_abort(q_ready, 0, abort, a.err);
+          for (int j = 0; ok && j < n_rel; ++j) {
+            if (!wait_or_abort(smem_u32(&sh->k_full[j % kKStages]), (j / kKStages) & 1, abort,
+                               a.err)) {
+              ok = false;
+              break;
+            }
             tc::fence_after_sync();
-            issue_pv(t, jp);
-            pv_next[t] = jp + 1;
-            progress = true;
-          }
-          const int js = s_next[t];
-          // S_t(js) overwrites the columns P_t(js - 1) lives in.  MMAs issued
-          // by one thread execute in issue order, so issuing it right after
-          // P_t(js - 1) V is enough; doing so at once makes the tensor-core
-          // order P0 V, S0, P1 V, S1 and offsets the two softmaxes by half a
-          // period, so one runs while the other tile's products do.
-          if (js < n_rel && pv_next[t] == js &&
-              mbar_test(smem_u32(&sh->k_full[js % kKStages]), (js / kKStages) & 1)) {
+            TC_MARK(300 + 64 * t + (j & 63));
+            issue_s(t, j);
+            tc::commit(smem_u32(&sh->k_empty[j % kKStages]));
+            if (!wait_or_abort(smem_u32(&sh->p_full[t]), j & 1, abort, a.err) ||
+                !wait_or_abort(smem_u32(&sh->v_full[j % kVStages]), (j / kVStages) & 1, abort,
+                               a.err)) {
+              ok = false;
+              break;
+            }
             tc::fence_after_sync();
-            issue_s(t, js);
-            s_next[t] = js + 1;
-            progress = true;
+            TC_MARK(500 + 64 * t + (j & 63));
+            issue_pv(t, j);
+            tc::commit(smem_u32(&sh->v_empty[j % kVStages]));
+          }
+          tc::commit(drain);
+          (void)mbar_wait(drain, 0);
+        }
+      } else {
+        // Event loop: issue whichever MMA is ready, never blocking on one
+        // query tile while the other could use the tensor core.  No barrier
+        // phase can run more than one ahead of what this thread has seen, so
+        // parity probes are unambiguous.
+        int s_next[kTcTiles] = {0, 0};   // next tile index whose S is issued
+        int pv_next[kTcTiles] = {0, 0};  // next tile index whose P V is issued
+        int k_released = 0, v_released = 0;  // ring stages handed back to the producer
+        bool ok = wait_or_abort(q_ready, 0, abort, a.err);
+        uint64_t idle_since = 0;
+        while (ok) {
+          bool progress = false;
+  #pragma unroll
+          for (int t = 0; t < kTcTiles; ++t) {   // (unrolled: the counters stay in registers)
+            if (t >= ntq) break;
+            const int jp = pv_next[t];
+            if (jp < s_next[t] && mbar_test(smem_u32(&sh->p_full[t]), jp & 1) &&
+                mbar_test(smem_u32(&sh->v_full[jp % kVStages]), (jp / kVStages) & 1)) {
+              tc::fence_after_sync();
+              TC_MARK(500 + 64 * t + (jp & 63));
+              issue_pv(t, jp);
+              pv_next[t] = jp + 1;
+              progress = true;
+            }
+            const int js = s_next[t];
+            // S_t(js) overwrites the columns P_t(js - 1) lives in.  MMAs issued
+            // by one thread execute in issue order, so issuing it right after
+            // P_t(js - 1) V is enough; doing so at once makes the tensor-core
+            // order P0 V, S0, P1 V, S1 and offsets the two softmaxes by half a
+            // period, so one runs while the other tile's products do.
+            if (js < n_rel && pv_next[t] == js &&
+                mbar_test(smem_u32(&sh->k_full[js % kKStages]), (js / kKStages) & 1)) {
+              tc::fence_after_sync();
+              TC_MARK(300 + 64 * t + (js & 63));
+              issue_s(t, js);
+              s_next[t] = js + 1;
+              progress = true;
+            }
+          }
+          int done_s = s_next[0], done_pv = pv_next[0];
+          if (ntq > 1) {
+            done_s = min(done_s, s_next[1]);
+            done_pv = min(done_pv, pv_next[1]);
+          }
+          while (k_released < done_s) {  // both S products of that K tile issued
+            tc::commit(smem_u32(&sh->k_empty[k_released % kKStages]));
+            ++k_released;
+          }
+          while (v_released < done_pv) {  // both P V products of that V tile issued
+            tc::commit(smem_u32(&sh->v_empty[v_released % kVStages]));
+            ++v_released;
+          }
+          if (done_pv == n_rel) break;
+          if (progress) {
+            idle_since = 0;
+          } else {
+            const uint64_t now = global_timer_ns();
+            if (idle_since == 0) {
+              idle_since = now;
+            } else if (*abort) {
+              ok = false;
+            } else if (now - idle_since > kWaitLimitNs) {
+              *abort = 1;
+              raise_error(a.err, PKV_ERR_TIMEOUT);
+              ok = false;
+            }
           }
         }
-        int done_s = s_next[0], done_pv = pv_next[0];
-        if (ntq > 1) {
-          done_s = min(done_s, s_next[1]);
-          done_pv = min(done_pv, pv_next[1]);
-        }
-        while (k_released < done_s) {  // both S products of that K tile issued
-          tc::commit(smem_u32(&sh->k_empty[k_released % kKStages]));
-          ++k_released;
-        }
-        while (v_released < done_pv) {  // both P V products of that V tile issued
-          tc::commit(smem_u32(&sh->v_empty[v_released % kVStages]));
-          ++v_released;
-        }
-        if (done_pv == n_rel) break;
-        if (progress) {
-          idle_since = 0;
-        } else {
-          const uint64_t now = global_timer_ns();
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (*abort) {
-            ok = false;
-          } else if (now - idle_since > kWaitLimitNs) {
-            *abort = 1;
-            raise_error(a.err, PKV_ERR_TIMEOUT);
-            ok = false;
-          }
-        }
+        // Every MMA issued here must finish before TMEM is released.
+        tc::commit(drain);
+        (void)mbar_wait(drain, 0);
       }
-      // Every MMA issued here must finish before TMEM is released.
-      tc::commit(drain);
-      (void)mbar_wait(drain, 0);
     }
     __syncwarp();
-  } else if (FP8 && warp >= 10) {
+   } else if (FP8 && warp >= 10) {
     // ------------------------------------------------- widen e4m3 tiles (FP8)
     const bool is_v = warp == 11;
     for (int i = 0; i < n_rel; ++i) {
@@ -554,9 +687,11 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(is_v ? &sh->v_full[st] : &sh->k_full[st]));
     }
+   }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) >> 2;                // query tile of this warpgroup
+    set_max_regs_inc_softmax();
+    const int t = warp >> 2;                      // query tile of this warpgroup
     const int quarter = warp & 3;                 // TMEM lanes this warp may touch
     const int row = quarter * 32 + lane;          // tile row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -564,7 +699,7 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
     const int g = row % G;
     const bool valid = tok <= tok_last;
     const int pos = casc ? L - 1 : L - qn + (valid ? tok : tok_last);
-    const int ts = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the warpgroup
+    const int ts = (warp & 3) * 32 + lane;        // 0..127 within the warpgroup
     const uint32_t b_sfull = smem_u32(&sh->s_full[t]);
     const uint32_t b_pfull = smem_u32(&sh->p_full[t]), b_pvdone = smem_u32(&sh->pv_done[t]);
     const uint32_t tS = tmem + lane_off + col_s(t), tP = tmem + lane_off + col_p(t);
@@ -616,6 +751,7 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
       // S_t(j) complete (its commit also covers P_t(j - 1) V, so O_t is stable)
       if (!warp_wait(b_sfull, j & 1, abort, a.err)) { done = false; break; }
       tc::fence_after_sync();
+      if (quarter == 0 && lane == 0) TC_MARK(700 + 64 * t + (j & 63));
       float x[kTcKeys];
 #pragma unroll
       for (int c0 = 0; c0 < kTcKeys; c0 += 32) {
@@ -674,8 +810,12 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
           const int k = 2 * (c0 + c);
           float y0, y1;
           tc::fma_f32x2(x[k], x[k + 1], m2, b2, y0, y1);
-          y0 = ex2(y0);
-          y1 = ex2(y1);
+          if ((c & 7) < kEmuPairs) {
+            tc::exp2_poly_x2(y0, y1);
+          } else {
+            y0 = ex2(y0);
+            y1 = ex2(y1);
+          }
           pk[c] = pack2<FP8>(y0, y1);
           tc::add_f32x2(acc[c & 3], y0, y1);
         }
@@ -711,6 +851,7 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pfull);
+      if (quarter == 0 && lane == 0) TC_MARK(900 + 64 * t + (j & 63));
     }
     if (done && casc && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
       // cascade prefix: the row's normalised partial and log2-sum-exp (in the
@@ -758,11 +899,25 @@ __global__ void __launch_bounds__(FP8 ? kTcThreadsFp8 : kTcThreads, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  TC_MARK(1);
+  if (warp == 9) {
     tc::fence_after_sync();
     tc::dealloc(tmem, kTmemCols);
   }
 }
+
+#ifdef PKV_TC_TIMELINE
+}  // namespace
+extern "C" int pkv_tc_timeline(unsigned long long* host, int n) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, g_tc_timeline,
+                                               sizeof(unsigned long long) * (n < 4096 ? n : 4096)));
+}
+extern "C" int pkv_tc_timeline_clear() {
+  static unsigned long long zeros[4096];
+  return static_cast<int>(cudaMemcpyToSymbol(g_tc_timeline, zeros, sizeof(zeros)));
+}
+namespace {
+#endif
 
 template <int D, bool FP8>
 cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -778,7 +933,7 @@ cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const 
                                         (a.prefix_tiles * kTcKeys)
                                   : a.num_seqs;
   dim3 grid(a.num_mtiles, a.num_kv_heads, gz);
-  kfn<<<grid, FP8 ? kTcThreadsFp8 : kTcThreads, smem, stream>>>(qmap, kmap, vmap, a);
+  kfn<<<grid, kTcThreads, smem, stream>>>(qmap, kmap, vmap, a);
   return cudaGetLastError();
 }
 

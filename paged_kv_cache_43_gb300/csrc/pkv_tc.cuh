@@ -55,6 +55,70 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Eight K-steps of one tile product in one instruction group:
+//   D (+)= sum over k < 8 of A_k * B_k,  A_k / B_k = the base descriptors
+//   advanced by OA_k / OB_k (16-byte units, immediates; address fields never
+//   carry out of the low word).  Only the first step reads `accumulate`; the
+//   others always accumulate.  One MMA costs a single tcgen05.mma plus two
+//   32-bit adds on the issuing thread: its instructions share the SM
+//   sub-partition's issue slots with busy softmax warps, so fewer of them
+//   keep the tensor core fed.
+template <int OA1, int OA2, int OA3, int OA4, int OA5, int OA6, int OA7, int OB1, int OB2, int OB3,
+          int OB4, int OB5, int OB6, int OB7>
+__device__ __forceinline__ void mma_ss_x8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b32 al, ah, bl, bh, x, y;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, 1, 1;\n\t"
+      "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.u32 x, al, %5;\n\tadd.u32 y, bl, %12;\n\tmov.b64 a, {x, ah};\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.u32 x, al, %6;\n\tadd.u32 y, bl, %13;\n\tmov.b64 a, {x, ah};\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.u32 x, al, %7;\n\tadd.u32 y, bl, %14;\n\tmov.b64 a, {x, ah};\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.u32 x, al, %8;\n\tadd.u32 y, bl, %15;\n\tmov.b64 a, {x, ah};\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.u32 x, al, %9;\n\tadd.u32 y, bl, %16;\n\tmov.b64 a, {x, ah};\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.u32 x, al, %10;\n\tadd.u32 y, bl, %17;\n\tmov.b64 a, {x, ah};\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+      "add.u32 x, al, %11;\n\tadd.u32 y, bl, %18;\n\tmov.b64 a, {x, ah};\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(OA1), "n"(OA2), "n"(OA3),
+      "n"(OA4), "n"(OA5), "n"(OA6), "n"(OA7), "n"(OB1), "n"(OB2), "n"(OB3), "n"(OB4), "n"(OB5),
+      "n"(OB6), "n"(OB7)
+      : "memory");
+}
+
+// The same with A in TMEM (columns a_tmem + 8k for step k) and B advanced by
+// 128 (2048 bytes) per step: the P V product of one 128-key tile.
+__device__ __forceinline__ void mma_ts_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b32 bl, bh, x, y;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, 1, 1;\n\t"
+      "mov.b64 {bl, bh}, %2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 x, %1, 8;\n\tadd.u32 y, bl, 128;\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t"
+      "add.u32 x, %1, 16;\n\tadd.u32 y, bl, 256;\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t"
+      "add.u32 x, %1, 24;\n\tadd.u32 y, bl, 384;\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t"
+      "add.u32 x, %1, 32;\n\tadd.u32 y, bl, 512;\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t"
+      "add.u32 x, %1, 40;\n\tadd.u32 y, bl, 640;\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t"
+      "add.u32 x, %1, 48;\n\tadd.u32 y, bl, 768;\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t"
+      "add.u32 x, %1, 56;\n\tadd.u32 y, bl, 896;\n\tmov.b64 b, {y, bh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {
@@ -147,6 +211,48 @@ __device__ __forceinline__ void add_f32x2(uint64_t& acc, float x0, float x1) {
   asm("{\n\t.reg .b64 a;\n\tmov.b64 a, {%1, %2};\n\tadd.rn.f32x2 %0, %0, a;\n\t}"
       : "+l"(acc)
       : "f"(x0), "f"(x1));
+}
+
+// Lane-wise (y0, y1) = 2^(y0, y1) on the FMA pipe instead of the MUFU (which
+// does 16 results per clock per SM, as many as the tensor core needs per
+// 128x128 score tile): Cody-Waite range reduction y = j + f with j the
+// nearest integer (adding 1.5 * 2^23 rounds y into the low mantissa bits) and
+// |f| <= 1/2, a degree-3 polynomial for 2^f, and j added to the exponent
+// field.  The coefficients are this library's own minimax fit of 2^f on
+// [-1/2, 1/2] by a Remez exchange on the relative error: at most 7.5e-5,
+// 26x below the bf16/fp16 rounding every weight goes through before the P V
+// product.  Inputs are clamped to -126 so that masked (-inf) scores give 0 or
+// a subnormal below 2^-125; inputs never exceed 2^8 here.
+constexpr float kExp2C0 = 0.99992806f;
+constexpr float kExp2C1 = 0.69326097f;
+constexpr float kExp2C2 = 0.24261113f;
+constexpr float kExp2C3 = 0.05517167f;
+constexpr float kExp2Round = 12582912.0f;   // 1.5 * 2^23
+
+__device__ __forceinline__ void exp2_poly_x2(float& y0, float& y1) {
+  const float a0 = fmaxf(y0, -126.f), a1 = fmaxf(y1, -126.f);
+  uint32_t t0, t1;
+  float p0, p1;
+  asm("{\n\t.reg .b64 a, m, t, j, f, p, c;\n\t"
+      "mov.b64 a, {%4, %5};\n\t"
+      "mov.b64 m, {%6, %6};\n\t"
+      "add.rn.f32x2 t, a, m;\n\t"
+      "sub.rn.f32x2 j, t, m;\n\t"
+      "sub.rn.f32x2 f, a, j;\n\t"
+      "mov.b64 c, {%7, %7};\n\t"
+      "mov.b64 p, {%8, %8};\n\t"
+      "fma.rn.f32x2 p, c, f, p;\n\t"
+      "mov.b64 c, {%9, %9};\n\t"
+      "fma.rn.f32x2 p, p, f, c;\n\t"
+      "mov.b64 c, {%10, %10};\n\t"
+      "fma.rn.f32x2 p, p, f, c;\n\t"
+      "mov.b64 {%0, %1}, p;\n\t"
+      "mov.b64 {%2, %3}, t;\n\t}"
+      : "=f"(p0), "=f"(p1), "=r"(t0), "=r"(t1)
+      : "f"(a0), "f"(a1), "f"(kExp2Round), "f"(kExp2C3), "f"(kExp2C2), "f"(kExp2C1),
+        "f"(kExp2C0));
+  y0 = __uint_as_float(__float_as_uint(p0) + (t0 << 23));
+  y1 = __uint_as_float(__float_as_uint(p1) + (t1 << 23));
 }
 
 __device__ __forceinline__ float sum_f32x2(uint64_t v) {
