@@ -79,6 +79,49 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak(sustained: bool = False):
+    """Measured dense bf16 tensor throughput (TFLOP/s): the burst figure for a
+    launch timed alone, the sustained one for a launch inside a long step."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(path) as f:
+            return float(json.load(f)[key]), "measured " + key
+    except Exception:
+        return (1700.0 if sustained else 1900.0), "fallback " + key
+
+
+def attention_flops(wl, seqs, window=0):
+    """4 * head_size flops per (query row, q head, visible key): the two
+    products of the attention definition (scores and weighted sum)."""
+    f = 0
+    for s in seqs:
+        L, n = int(wl.ctx_lens[s]), int(wl.q_lens[s])
+        vis = L - n + np.arange(n, dtype=np.int64) + 1       # keys 0 .. pos
+        if window > 0:
+            vis = np.minimum(vis, window)
+        f += int(vis.sum())
+    return f * wl.num_q_heads * 4 * wl.head_size
+
+
+def sub_batch(wl, s0, s1):
+    """Sequences [s0, s1) of a workload as a batch of their own over the same
+    caches (views of its tensors; query_start_loc rebased)."""
+    from paged_kv_cache_43_gb300 import workloads as W
+    qsl = wl.query_start_loc.cpu().numpy()
+    t0, t1 = int(qsl[s0]), int(qsl[s1])
+    out = W.Workload(**{k: getattr(wl, k) for k in wl.__dataclass_fields__})
+    for name in ("q", "k_new", "v_new", "slot_mapping"):
+        setattr(out, name, getattr(wl, name)[t0:t1])
+    out.block_tables = wl.block_tables[s0:s1]
+    out.context_lens = wl.context_lens[s0:s1]
+    out.query_start_loc = (wl.query_start_loc[s0:s1 + 1] - t0).contiguous()
+    out.q_lens, out.ctx_lens = wl.q_lens[s0:s1], wl.ctx_lens[s0:s1]
+    out.num_decode_seqs = max(0, min(wl.num_decode_seqs, s1) - s0)
+    out.shared_seqs = ()
+    return out
+
+
 def decode_source_hash() -> str:
     """sha256 over what the decode kernel is compiled from: its source, the
     common device header and its argument struct (DecodeArgs, the text of its
@@ -336,14 +379,33 @@ class KVCache:
         else:
             self.pkv.write(k_new, v_new, slots, self.k, self.v, stream=stream)
 
-    def attention(self, out, q, bt, cl, qsl, ws, stream, kd=None, vd=None):
+    def attention(self, out, q, bt, cl, qsl, ws, stream, kd=None, vd=None, meta_kw=None):
+        mk = self.meta_kw if meta_kw is None else meta_kw
         if self.fp8:
             self.pkv.attention_fp8(out, q, self.k, self.v, bt, cl, qsl, self.wl.scale,
                                    self.kd if kd is None else kd, self.vd if vd is None else vd,
-                                   workspace=ws, stream=stream, **self.meta_kw)
+                                   workspace=ws, stream=stream, **mk)
         else:
             self.pkv.attention(out, q, self.k, self.v, bt, cl, qsl, self.wl.scale,
-                               workspace=ws, stream=stream, **self.meta_kw)
+                               workspace=ws, stream=stream, **mk)
+
+    def part_timer(self, s0, s1, stream):
+        """A zero-argument call of pkv_attention on sequences [s0, s1) alone
+        (the caches already hold this step's tokens) and that part's batch."""
+        sub = sub_batch(self.wl, s0, s1)
+        mk = dict(self.meta_kw, max_query_len=sub.max_query_len,
+                  max_context_len=sub.max_context_len, num_decode_seqs=sub.num_decode_seqs)
+        meta = self.pkv.attn_meta(sub.q, sub.block_tables, sub.context_lens, **mk)
+        ws = torch.empty(max(self.pkv.workspace_size(self.k, meta), 1), dtype=torch.uint8,
+                         device=sub.q.device)
+        out = torch.empty_like(sub.q)
+        kd = self.kd[s0:s1].contiguous() if self.fp8 else None
+        vd = self.vd[s0:s1].contiguous() if self.fp8 else None
+
+        def call():
+            self.attention(out, sub.q, sub.block_tables, sub.context_lens, sub.query_start_loc,
+                           ws, stream, kd=kd, vd=vd, meta_kw=mk)
+        return call, sub
 
     def step(self, out, ws, stream):
         wl = self.wl
@@ -487,9 +549,124 @@ def run_pkv(args, rank, world, device):
         "e2e": e2e,
         "parity_max_abs_err": parity,
     }
+    if wl.num_decode_seqs < wl.num_seqs:
+        # a batch with prefill rows: its dense contraction bounds it
+        line["roofline"] = mixed_roofline(kv, stream, attn_ms, min(args.steps, 200),
+                                          args.window)
     if base_samples:
         line["cpu_baseline"] = cpu_baseline(base_samples, wl.name, wl.num_seqs, args.window)
+    if (world == 1 and args.workload == 2 and not args.window and not args.kv_split
+            and not args.num_seqs and args.kv_dtype == "bf16" and not args.no_per_workload):
+        # the other decode and mixed configurations, and the e4m3 cache, each
+        # measured briefly on the same GPU (not part of `value`)
+        steps = max(50, min(args.steps, 200))
+        line["per_workload"] = {
+            f"{W.WORKLOAD_NAMES[n]}{'-fp8' if f else ''}": workload_entry(n, f, device, steps, 10)
+            for n, f in PER_WORKLOAD}
     return line
+
+
+def mixed_roofline(kv, stream, attn_ms, steps, window=0):
+    """Roofline of a batch with decode and prefill rows: the prefill
+    sequences' call timed alone against the tensor peak (it is the dense
+    contraction: 4 D flops per row and visible key), the decode sequences'
+    call timed alone against the HBM bandwidth, and the whole call against
+    max(bytes / bandwidth, flops / tensor peak)."""
+    wl = kv.wl
+    nd, S = wl.num_decode_seqs, wl.num_seqs
+    hbm, hbm_kind = hbm_peak()
+    tpk, tpk_kind = tensor_peak(sustained=False)
+    pf_call, pf = kv.part_timer(nd, S, stream)
+    pf_ms = _time_calls(pf_call, steps, 5, stream)
+    pf_flops = attention_flops(wl, range(nd, S), window)
+    pf_bytes = algorithmic_bytes(pf, window, kv.fp8)[0]
+    res = {
+        "kernel": "pkv_prefill_tc_kernel: the prefill sequences' pkv_attention call timed "
+                  "alone (CUDA events)",
+        "bound": "tensor", "achieved": round(pf_flops / (pf_ms * 1e-3) / 1e12, 1),
+        "peak": tpk, "unit": "TFLOP/s",
+        "frac": round(pf_flops / (pf_ms * 1e-3) / 1e12 / tpk, 4),
+        "peak_kind": tpk_kind, "traffic": None,
+        "flops_per_launch": pf_flops, "launch_ms": round(pf_ms, 5),
+    }
+    total_flops = attention_flops(wl, range(S), window)
+    total_bytes = algorithmic_bytes(wl, window, kv.fp8)[0]
+    if nd:
+        dc_call, dc = kv.part_timer(0, nd, stream)
+        dc_ms = _time_calls(dc_call, steps, 5, stream)
+        dc_bytes = algorithmic_bytes(dc, window, kv.fp8)[0]
+        res["decode_half"] = {
+            "kernel": "split-K decode kernel + combine: the decode sequences' call timed alone",
+            "bound": "hbm", "achieved": round(dc_bytes / (dc_ms * 1e-3) / 1e9, 1),
+            "peak": hbm, "unit": "GB/s", "frac": round(dc_bytes / (dc_ms * 1e-3) / 1e9 / hbm, 4),
+            "peak_kind": f"{hbm_kind} hbm_gbs", "launch_ms": round(dc_ms, 5),
+            "algorithmic_bytes_per_launch": dc_bytes}
+    ideal_ms = max(total_bytes / (hbm * 1e9), total_flops / (tpk * 1e12)) * 1e3
+    res["whole_call"] = {
+        "attention_ms": round(attn_ms, 5), "ideal_ms": round(ideal_ms, 5),
+        "frac": round(ideal_ms / attn_ms, 4),
+        "ideal": "max(algorithmic bytes / HBM peak, flops / tensor peak)",
+        "algorithmic_bytes": total_bytes, "flops": total_flops}
+    return res
+
+
+def workload_entry(n, fp8, device, steps, warmup):
+    """One short measurement of workload n (rank-0 seed, automatic split):
+    step time (write + attention), attention time, its roofline (HBM for
+    decode batches; tensor for the prefill part of a mixed batch, with the
+    decode part's HBM fraction beside it) and a parity spot check."""
+    from paged_kv_cache_43_gb300 import pkv
+    from paged_kv_cache_43_gb300 import workloads as W
+    seed = rank_seed(n, 0)
+    wl = W.workload(n, device=device, seed=seed)
+    kv = KVCache(wl, fp8, seed, 0, 0)
+    attn_b, write_b, kv_b = algorithmic_bytes(wl, 0, fp8)
+    out = torch.empty_like(wl.q)
+    meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **kv.meta_kw)
+    ws = torch.empty(max(pkv.workspace_size(kv.k, meta), 1), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    spot = oracle_sample(wl, [int(np.argmin(wl.ctx_lens)), int(np.argmax(wl.ctx_lens))],
+                         fp8=kv.np_scales)
+    for _ in range(warmup):
+        kv.step(out, ws, stream)
+    torch.cuda.synchronize(device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        kv.write(wl.k_new, wl.v_new, wl.slot_mapping, stream)
+        e1.record(stream)
+        kv.attention(out, wl.q, wl.block_tables, wl.context_lens, wl.query_start_loc, ws, stream)
+        e2.record(stream)
+    torch.cuda.synchronize(device)
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / steps
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    if pkv.get_error(clear=True):
+        raise RuntimeError(f"device error word set ({wl.name})")
+    parity = spot_check(wl, out, spot)
+    peak, peak_kind = hbm_peak()
+    entry = {
+        "workload": wl.name, "kv_cache_dtype": "fp8_e4m3" if fp8 else "bf16", "steps": steps,
+        "ms_per_step": round(step_ms, 5), "attention_ms": round(attn_ms, 5),
+        "kv_gbs_step": round((attn_b + write_b) / (step_ms * 1e-3) / 1e9, 1),
+        "decode_tokens_per_s": round(wl.num_tokens / (step_ms * 1e-3), 1),
+        "parity_max_abs_err": parity,
+    }
+    if wl.num_decode_seqs < wl.num_seqs:
+        entry["roofline"] = mixed_roofline(kv, stream, attn_ms, steps)
+    else:
+        achieved = attn_b / (attn_ms * 1e-3) / 1e9
+        entry["roofline"] = {
+            "kernel": "pkv_attention (split-K decode kernel + combine), CUDA events per call",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+            "traffic": recorded_traffic(wl.name + ("-fp8" if fp8 else "")),
+            "algorithmic_bytes_per_launch": attn_b}
+    del kv, wl, out, ws
+    torch.cuda.empty_cache()
+    return entry
+
+
+PER_WORKLOAD = [(3, False), (4, False), (5, False), (2, True), (3, True), (4, True), (5, True)]
 
 
 def profile_only(args, kv):
@@ -525,9 +702,15 @@ def spot_check(wl, out, spot, window=0):
 
 def end_to_end(kv, args, stream, device, step_bytes):
     """Same metric through the public calls with host-resident step inputs:
-    pinned H2D of q, new K/V, slots and metadata (and the descales of an e4m3
-    cache), the step, D2H of out.  The step's inputs sit in one pinned staging
-    buffer and go over in one copy; the calls take views of its device twin."""
+    every step copies its inputs -- q, new K/V, slots and metadata (and the
+    descales of an e4m3 cache) -- from pinned host memory to the device, runs
+    the write and the attention on them, and copies its output back to pinned
+    host memory.  A step's inputs sit in one pinned staging buffer and go over
+    in one copy.  The copies run on their own streams into double-buffered
+    device staging, event-joined with the compute stream, so that step i + 1's
+    inputs go up (and step i - 1's output comes down) while step i computes, as
+    a serving loop stages its next batch ahead; every copy of the n timed
+    steps is inside the timed region."""
     from paged_kv_cache_43_gb300 import pkv
     wl = kv.wl
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
@@ -541,45 +724,68 @@ def end_to_end(kv, args, stream, device, step_bytes):
         offs[n] = (total, nbytes)
         total += (nbytes + 255) // 256 * 256
     host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=device)
     for n, t in src.items():
         o, nb = offs[n]
         host_buf[o:o + nb].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
-    dev = {n: dev_buf[o:o + nb].view(src[n].dtype).view(src[n].shape)
-           for n, (o, nb) in offs.items()}
-    out_h = torch.empty(wl.q.shape, dtype=wl.q.dtype).pin_memory()
-    out_d = torch.empty_like(wl.q)
+    dev_bufs = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(2)]
+    dev = [{n: b[o:o + nb].view(src[n].dtype).view(src[n].shape)
+            for n, (o, nb) in offs.items()} for b in dev_bufs]
+    out_h = [torch.empty(wl.q.shape, dtype=wl.q.dtype).pin_memory() for _ in range(2)]
+    out_d = [torch.empty_like(wl.q) for _ in range(2)]
     h2d = sum(nb for _, nb in offs.values())
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = out_h[0].numel() * out_h[0].element_size()
     meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **kv.meta_kw)
     ws = torch.empty(max(pkv.workspace_size(kv.k, meta), 1), dtype=torch.uint8,
                      device=device)
+    up = torch.cuda.Stream(device)      # host -> device
+    down = torch.cuda.Stream(device)    # device -> host
+    ev = lambda: torch.cuda.Event()     # noqa: E731
+    copied, done, drained = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            dev_buf.copy_(host_buf, non_blocking=True)
-        kv.write(dev["k_new"], dev["v_new"], dev["slot_mapping"], stream)
-        kv.attention(out_d, dev["q"], dev["block_tables"], dev["context_lens"],
-                     dev["query_start_loc"], ws, stream, kd=dev.get("k_descale"),
-                     vd=dev.get("v_descale"))
-        with torch.cuda.stream(stream):
-            out_h.copy_(out_d, non_blocking=True)
+    def run(n, t_start=None):
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        with torch.cuda.stream(up):
+            dev_bufs[0].copy_(host_buf, non_blocking=True)
+            copied[0].record(up)
+        for i in range(n):
+            b, nb = i % 2, (i + 1) % 2
+            if i + 1 < n:   # the next step's inputs, once step i - 1 is done with them
+                if i >= 1:
+                    up.wait_event(done[nb])
+                with torch.cuda.stream(up):
+                    dev_bufs[nb].copy_(host_buf, non_blocking=True)
+                    copied[nb].record(up)
+            stream.wait_event(copied[b])
+            if i >= 2:
+                stream.wait_event(drained[b])   # step i - 2's output has left out_d[b]
+            d = dev[b]
+            kv.write(d["k_new"], d["v_new"], d["slot_mapping"], stream)
+            kv.attention(out_d[b], d["q"], d["block_tables"], d["context_lens"],
+                         d["query_start_loc"], ws, stream, kd=d.get("k_descale"),
+                         vd=d.get("v_descale"))
+            done[b].record(stream)
+            down.wait_event(done[b])
+            with torch.cuda.stream(down):
+                out_h[b].copy_(out_d[b], non_blocking=True)
+                drained[b].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
 
     n = max(args.steps // 4, 10)
-    for _ in range(3):
-        e2e_step()
+    run(3)
     torch.cuda.synchronize(device)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(n):
-        e2e_step()
+    run(n)
     b.record(stream)
     torch.cuda.synchronize(device)
     ms = a.elapsed_time(b) / n
     return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
-            "steps": n}
+            "steps": n, "copies": "each step's inputs H2D and output D2H, on two copy "
+                                  "streams overlapping the neighbouring steps' compute"}
 
 
 def _time_calls(fn, steps, warmup, stream):
@@ -854,6 +1060,8 @@ def main():
                     help="cache storage: the workload's bf16, or e4m3 codes with per-kv-head "
                          "scales (workloads 2-5)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the short per-workload measurements of the default run")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="override the batch size (profiling captures on a smaller case)")
     ap.add_argument("--cascade-bench", action="store_true",

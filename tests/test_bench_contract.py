@@ -48,3 +48,28 @@ def test_pool_bench_runs_on_the_host():
 def test_fewer_than_three_warmup_steps_are_refused():
     r = run("--impl", "reference", "--workload", "1", "--steps", "3", "--warmup", "2")
     assert r.returncode != 0
+
+
+def test_mixed_batch_parts_and_flops():
+    """The bench's split of a mixed batch into its decode and prefill parts
+    (views over the same caches) and its flop count (4 D per row and visible
+    key, the window capping the keys a row sees)."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_cache_43_gb300 import workloads as W
+    wl = W.make_workload([1, 1, 5, 3], [40, 17, 30, 3], num_q_heads=4, num_kv_heads=2,
+                         head_size=64, seed=3)
+    assert wl.num_decode_seqs == 2
+    dec, pf = bench.sub_batch(wl, 0, 2), bench.sub_batch(wl, 2, 4)
+    assert dec.num_decode_seqs == 2 and pf.num_decode_seqs == 0
+    assert pf.query_start_loc.tolist() == [0, 5, 8] and pf.q.shape[0] == 8
+    assert pf.q.data_ptr() == wl.q[2:].data_ptr() and pf.k_cache is wl.k_cache
+    assert pf.block_tables.tolist() == wl.block_tables[2:].tolist()
+    # rows of seq 2 see 26..30 keys, of seq 3 see 1..3 keys
+    keys = sum(range(26, 31)) + sum(range(1, 4))
+    assert bench.attention_flops(wl, [2, 3]) == keys * 4 * 4 * 64
+    assert bench.attention_flops(wl, [0, 1]) == (40 + 17) * 4 * 4 * 64
+    keys_w = sum(min(k, 4) for k in range(26, 31)) + sum(range(1, 4))
+    assert bench.attention_flops(wl, [2, 3], window=4) == keys_w * 4 * 4 * 64
+    assert np.array_equal(pf.ctx_lens, wl.ctx_lens[2:])
