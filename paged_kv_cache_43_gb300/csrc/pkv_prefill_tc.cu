@@ -74,10 +74,12 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kTcThreads * 168, "re
 #define PKV_TC_EMU_PAIRS 0
 #endif
 constexpr int kEmuPairs = PKV_TC_EMU_PAIRS;
-// bf16: one MMA-issuing thread per query tile (1) or one for both (0).
-#ifndef PKV_TC_TWO_ISSUERS
-#define PKV_TC_TWO_ISSUERS 0
+// Each softmax warpgroup issues its own tile's MMAs (1), or warp 9 issues
+// both tiles' from an event loop (0).
+#ifndef PKV_TC_SELF_ISSUE
+#define PKV_TC_SELF_ISSUE 1
 #endif
+constexpr bool kSelfIssue = PKV_TC_SELF_ISSUE != 0;
 #ifndef PKV_TC_KSTAGES
 #define PKV_TC_KSTAGES 3
 #endif
@@ -108,6 +110,7 @@ struct TcShared {
   uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t k_land[kKStages], v_land[kVStages];   // FP8: codes landed, not yet widened
+  uint64_t issued[kTcTiles];   // tile t's issuer has issued its next MMA group
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -385,15 +388,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tensor_map(&kmap);
     prefetch_tensor_map(&vmap);
     mbar_init(q_full, 1);
-    // bf16: one MMA-issuing thread per query tile, each committing its own
-    // products (FP8: one thread issues both tiles' products)
-    const uint32_t issuers = (FP8 || !PKV_TC_TWO_ISSUERS) ? 1u : static_cast<uint32_t>(ntq);
+    // one MMA-issuing thread per query tile, each committing its own
+    // products (or one thread issuing both tiles')
+    const uint32_t issuers = kSelfIssue ? static_cast<uint32_t>(ntq) : 1u;
     mbar_init(drain, issuers);
     mbar_init(smem_u32(&sh->q_conv), 8);   // one arrival per softmax warp
     for (int t = 0; t < kTcTiles; ++t) {
       mbar_init(smem_u32(&sh->s_full[t]), 1);
       mbar_init(smem_u32(&sh->p_full[t]), 4);
       mbar_init(smem_u32(&sh->pv_done[t]), 1);
+      mbar_init(smem_u32(&sh->issued[t]), 1);
     }
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(smem_u32(&sh->k_full[i]), 1);
@@ -415,6 +419,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = sh->tmem_base;
   volatile int32_t* abort = &sh->abort;
   TC_MARK(0);
+#ifdef PKV_TC_TIMELINE
+  const int cta_lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  if (threadIdx.x == 0 && cta_lin < 600) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_tc_timeline[2048 + 3 * cta_lin] = smid;
+    g_tc_timeline[2048 + 3 * cta_lin + 1] = global_timer_ns();
+  }
+#endif
+
+  // ---------------------------------------------------------- MMA issue
+  constexpr uint32_t idS = FP8 ? tc::idesc_f16_f32(kTcRows, kTcKeys, 0, 0)
+                               : tc::idesc_bf16_f32(kTcRows, kTcKeys, 0, 0);
+  constexpr uint32_t idO = FP8 ? tc::idesc_f16_f32(kTcRows, D, 0, 1)
+                               : tc::idesc_bf16_f32(kTcRows, D, 0, 1);
+  // Shared-memory descriptors are built once: the address field is the
+  // low 14 bits (address / 16) and never carries, so an operand at a
+  // constant byte offset is the base descriptor plus offset / 16 -- one
+  // add per MMA on the issuing thread, whose instructions compete with
+  // the softmax warps for the same issue slots.
+  const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(sQ), 16, 1024);
+  const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(sK), 16, 1024);
+  const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(sV), Lt::kKvHalf, 1024);
+  auto issue_s = [&](int t, int j) {
+    const uint64_t da0 = dq0 + static_cast<uint64_t>((t * Lt::kQTile) >> 4);
+    const uint64_t db0 = dk0 + static_cast<uint64_t>(((j % kKStages) * Lt::kTileBytes) >> 4);
+    const uint32_t d = tmem + col_s(t);
+    // K-step k: 16 bf16 = 32 B along the swizzled 128-B row, 64 columns
+    // per half (16 KB apart for both operands)
+    static_assert(Lt::kQHalf == Lt::kKvHalf, "equal half strides");
+    if constexpr (D == 128) {
+      tc::mma_ss_x8<2, 4, 6, 1024, 1026, 1028, 1030, 2, 4, 6, 1024, 1026, 1028, 1030>(
+          d, da0, db0, idS, 0u);
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc::mma_ss(d, da0 + (kk * 32 >> 4), db0 + (kk * 32 >> 4), idS, kk > 0 ? 1u : 0u);
+    }
+    tc::commit(smem_u32(&sh->s_full[t]));
+  };
+  auto issue_pv = [&](int t, int j) {
+    const uint64_t db0 = dv0 + static_cast<uint64_t>(((j % kVStages) * Lt::kTileBytes) >> 4);
+    tc::mma_ts_x8(tmem + col_o(t), tmem + col_p(t), db0, idO, j > 0 ? 1u : 0u);
+    tc::commit(smem_u32(&sh->pv_done[t]));
+  };
+
 
   if (warp >= 8) {
    set_max_regs_dec_other();
@@ -527,80 +577,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-   } else if (warp == 9 || (!FP8 && PKV_TC_TWO_ISSUERS && warp == 11)) {
+   } else if (warp == 9 && !kSelfIssue) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idS = FP8 ? tc::idesc_f16_f32(kTcRows, kTcKeys, 0, 0)
-                                   : tc::idesc_bf16_f32(kTcRows, kTcKeys, 0, 0);
-      constexpr uint32_t idO = FP8 ? tc::idesc_f16_f32(kTcRows, D, 0, 1)
-                                   : tc::idesc_bf16_f32(kTcRows, D, 0, 1);
-      // Shared-memory descriptors are built once: the address field is the
-      // low 14 bits (address / 16) and never carries, so an operand at a
-      // constant byte offset is the base descriptor plus offset / 16 -- one
-      // add per MMA on the issuing thread, whose instructions compete with
-      // the softmax warps for the same issue slots.
-      const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(sV), Lt::kKvHalf, 1024);
-      auto issue_s = [&](int t, int j) {
-        const uint64_t da0 = dq0 + static_cast<uint64_t>((t * Lt::kQTile) >> 4);
-        const uint64_t db0 = dk0 + static_cast<uint64_t>(((j % kKStages) * Lt::kTileBytes) >> 4);
-        const uint32_t d = tmem + col_s(t);
-        // K-step k: 16 bf16 = 32 B along the swizzled 128-B row, 64 columns
-        // per half (16 KB apart for both operands)
-        static_assert(Lt::kQHalf == Lt::kKvHalf, "equal half strides");
-        if constexpr (D == 128) {
-          tc::mma_ss_x8<2, 4, 6, 1024, 1026, 1028, 1030, 2, 4, 6, 1024, 1026, 1028, 1030>(
-              d, da0, db0, idS, 0u);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc::mma_ss(d, da0 + (kk * 32 >> 4), db0 + (kk * 32 >> 4), idS, kk > 0 ? 1u : 0u);
-        }
-        tc::commit(smem_u32(&sh->s_full[t]));
-      };
-      auto issue_pv = [&](int t, int j) {
-        const uint64_t db0 = dv0 + static_cast<uint64_t>(((j % kVStages) * Lt::kTileBytes) >> 4);
-        tc::mma_ts_x8(tmem + col_o(t), tmem + col_p(t), db0, idO, j > 0 ? 1u : 0u);
-        tc::commit(smem_u32(&sh->pv_done[t]));
-      };
-      if constexpr (!FP8 && PKV_TC_TWO_ISSUERS) {
-        // One issuing thread per query tile (warp 9: tile 0, warp 11: tile
-        // 1), on different SM sub-partitions: a single issuer shares its
-        // sub-partition's issue slots with two busy softmax warps and is
-        // starved by them (measured on GB300: an issuing thread beside one
-        // FMA-bound warp gets an MMA out every ~240 cycles instead of 64).
-        // Per tile the order is S(0), P(0) V, S(1), P(1) V, ...: S(j + 1)
-        // overwrites the columns P(j) lives in, and one thread's MMAs execute
-        // in issue order.
-        const int t = warp == 9 ? 0 : 1;
-        if (t < ntq) {
-          bool ok = wait_or_abort(q_ready, 0, abort, a.err);
-          for (int j = 0; ok && j < n_rel; ++j) {
-            if (!wait_or_abort(smem_u32(&sh->k_full[j % kKStages]), (j / kKStages) & 1, abort,
-                               a.err)) {
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-            TC_MARK(300 + 64 * t + (j & 63));
-            issue_s(t, j);
-            tc::commit(smem_u32(&sh->k_empty[j % kKStages]));
-            if (!wait_or_abort(smem_u32(&sh->p_full[t]), j & 1, abort, a.err) ||
-                !wait_or_abort(smem_u32(&sh->v_full[j % kVStages]), (j / kVStages) & 1, abort,
-                               a.err)) {
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-            TC_MARK(500 + 64 * t + (j & 63));
-            issue_pv(t, j);
-            tc::commit(smem_u32(&sh->v_empty[j % kVStages]));
-          }
-          tc::commit(drain);
-          (void)mbar_wait(drain, 0);
-        }
-      } else {
+      {
         // Event loop: issue whichever MMA is ready, never blocking on one
         // query tile while the other could use the tensor core.  No barrier
         // phase can run more than one ahead of what this thread has seen, so
@@ -747,6 +727,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool done = t < ntq;
     const int lo = a.window > 0 ? pos - a.window + 1 : 0;  // first key in this row's window
+    // Thread 0 of the warpgroup issues its tile's MMAs.  Handing them to
+    // a separate MMA warp costs a wake-up per product, and that warp, sharing
+    // its SM sub-partition with two softmax warps that have instructions ready
+    // most of the time, gets few issue slots (measured on GB300: an issuing
+    // thread beside one FMA-bound warp gets an MMA out every ~240 cycles
+    // instead of 64).  Per tile the order is S(0), P(0) V, S(1), P(1) V, ...:
+    // S(j + 1) overwrites the columns P(j) lives in, and one thread's MMAs
+    // execute in issue order.
+    // The two tiles' issuers take turns -- S0(0), S1(0), then groups
+    // [P0(j) V, S0(j + 1)], [P1(j) V, S1(j + 1)], ... -- so that each tile's
+    // softmax runs while the tensor core works on the other tile's products
+    // (left to themselves the two tiles fall into step and their softmaxes
+    // contend).  issued[t] completes one phase per group tile t has issued,
+    // its S(0) being phase 0; a turn waits for the other tile's previous
+    // group, which cannot run two phases ahead of the waiter.
+    constexpr bool self_issue = kSelfIssue;
+    const bool issuer = self_issue && done && quarter == 0 && lane == 0;
+    const bool paired = ntq > 1;
+    const uint32_t my_issued = smem_u32(&sh->issued[t]);
+    const uint32_t other_issued = smem_u32(&sh->issued[t ^ 1]);
+    if (issuer) {
+      if (wait_or_abort(q_ready, 0, abort, a.err) &&
+          wait_or_abort(smem_u32(&sh->k_full[0]), 0, abort, a.err) &&
+          (t == 0 || wait_or_abort(other_issued, 0, abort, a.err))) {
+        tc::fence_after_sync();
+        TC_MARK(300 + 64 * t);
+        issue_s(t, 0);
+        tc::commit(smem_u32(&sh->k_empty[0]));
+        mbar_arrive(my_issued);
+      }
+    }
+    __syncwarp();
     for (int j = 0; done && j < n_rel; ++j) {
       // S_t(j) complete (its commit also covers P_t(j - 1) V, so O_t is stable)
       if (!warp_wait(b_sfull, j & 1, abort, a.err)) { done = false; break; }
@@ -852,7 +864,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pfull);
       if (quarter == 0 && lane == 0) TC_MARK(900 + 64 * t + (j & 63));
+      if (issuer) {
+        // (a failed wait leaves the other warps to give up on s_full)
+        // this tile's group j: after the other tile's group j - 1 (tile 0)
+        // or group j (tile 1), i.e. the other barrier's phase j or j + 1
+        if (wait_or_abort(b_pfull, j & 1, abort, a.err) &&
+            wait_or_abort(smem_u32(&sh->v_full[j % kVStages]), (j / kVStages) & 1, abort,
+                          a.err) &&
+            (!paired || wait_or_abort(other_issued, (j + t) & 1, abort, a.err))) {
+          tc::fence_after_sync();
+          TC_MARK(500 + 64 * t + (j & 63));
+          issue_pv(t, j);
+          tc::commit(smem_u32(&sh->v_empty[j % kVStages]));
+          const int jn = j + 1;
+          if (jn < n_rel && wait_or_abort(smem_u32(&sh->k_full[jn % kKStages]),
+                                          (jn / kKStages) & 1, abort, a.err)) {
+            tc::fence_after_sync();
+            TC_MARK(300 + 64 * t + (jn & 63));
+            issue_s(t, jn);
+            tc::commit(smem_u32(&sh->k_empty[jn % kKStages]));
+          }
+          mbar_arrive(my_issued);
+        }
+      }
+      __syncwarp();
     }
+    if (issuer) {   // every MMA this thread issued completes before TMEM is freed
+      tc::commit(drain);
+      (void)mbar_wait(drain, 0);
+    }
+    __syncwarp();
     if (done && casc && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
       // cascade prefix: the row's normalised partial and log2-sum-exp (in the
       // scaled log2 domain of m_used) for the merge
@@ -900,6 +941,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   TC_MARK(1);
+#ifdef PKV_TC_TIMELINE
+  if (threadIdx.x == 0 && cta_lin < 600) g_tc_timeline[2048 + 3 * cta_lin + 2] = global_timer_ns();
+#endif
   if (warp == 9) {
     tc::fence_after_sync();
     tc::dealloc(tmem, kTmemCols);
