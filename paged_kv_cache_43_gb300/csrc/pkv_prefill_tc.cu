@@ -223,6 +223,25 @@ __device__ __forceinline__ void widen_tile_fp8(uint8_t* tile, int lane) {
   __syncwarp();
 }
 
+// Zeroes the V rows [0, lead) and [tail, 128) of one landed 128-key tile
+// (bf16 or widened fp16 layout: D / 64 halves of 128 rows x 128 B, 16 KB
+// apart); the calling warp's 32 lanes share the stores.  Those keys have
+// P = 0 in every row, but their rows may hold stale data -- NaN included --
+// which 0 * NaN would carry into P V.
+template <int D>
+__device__ __forceinline__ void zero_v_rows(uint8_t* vt, int lead, int tail, int lane) {
+  constexpr int per_row = (D / 64) * 8;   // 16-byte chunks per row
+  const int nlead = lead > 0 ? lead : 0;
+  const int ntail = kTcKeys - tail;
+  for (int e = lane; e < (nlead + ntail) * per_row; e += 32) {
+    const int r = e / per_row;
+    const int key = r < nlead ? r : tail + (r - nlead);
+    const int rem = e % per_row;
+    *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kTcKeys * 128) + key * 128 + (rem & 7) * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // Which (sequence, row-tile pair, kv head) this CTA computes.  The block
 // scheduler starts CTAs in launch order, so with `longest_first` the grid is
 // handed out longest first (list scheduling): the units (sequence, pair) are
@@ -379,6 +398,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int lo_min = a.window > 0 ? pos_min - a.window + 1 : 0;
   const int b_lo = casc ? j0 * (kTcKeys / kBlock) : (lo_min > 0 ? lo_min / kBlock : 0);
   const int nblk = (pos_max + kBlock) / kBlock;
+  // V rows of the first tile before the first loaded block, and of the last
+  // tile past pos_max, are zeroed once the tile has landed (zero_v_rows).
+  const int v_lead = min(kTcKeys, b_lo * kBlock - j0 * kTcKeys);
+  const int v_tail = pos_max + 1 - (ntiles - 1) * kTcKeys;
+  auto v_edges = [&](int rel, int& lead, int& tail) {
+    lead = rel == 0 ? v_lead : 0;
+    tail = rel == n_rel - 1 ? v_tail : kTcKeys;
+    return lead > 0 || tail < kTcKeys;
+  };
 
   const uint32_t q_full = smem_u32(&sh->q_full), drain = smem_u32(&sh->drain);
   // the MMAs may read Q once it has landed (bf16) or been converted (FP8)
@@ -533,6 +561,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if constexpr (!FP8) {
       const bool is_v = warp == 10;
       const int stages = is_v ? kVStages : kKStages;
+      uint32_t land_phase = 0;   // parity of each stage's next v_land phase
       for (int rel = 0; rel < n_rel; ++rel) {
         if (rel > 0 && (rel & 3) == 0) {
           g_cur = g_nxt;
@@ -543,10 +572,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             !warp_wait(smem_u32(is_v ? &sh->v_empty[st] : &sh->k_empty[st]),
                        ((rel / stages) - 1) & 1, abort, a.err))
           break;
+        int lead, tail;
+        const bool edge = is_v && v_edges(rel, lead, tail);
         issue_tile(j0 + rel, g_cur, rel & 3, is_v,
                    smem_u32((is_v ? sV : sK) + st * Lt::kTileBytes),
-                   smem_u32(is_v ? &sh->v_full[st] : &sh->k_full[st]));
+                   smem_u32(edge ? &sh->v_land[st] : is_v ? &sh->v_full[st] : &sh->k_full[st]));
         if (lane == 0) TC_MARK((is_v ? 200 : 100) + (rel & 63));
+        if (edge) {   // landed, edge rows zeroed, then full
+          if (!warp_wait(smem_u32(&sh->v_land[st]), (land_phase >> st) & 1u, abort, a.err))
+            break;
+          land_phase ^= 1u << st;
+          zero_v_rows<D>(sV + st * Lt::kTileBytes, lead, tail, lane);
+          fence_proxy_async();   // generic writes, then the tensor core reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sh->v_full[st]));
+        }
       }
     } else {
       for (int rel = 0; rel <= n_rel; ++rel) {
@@ -663,6 +703,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!warp_wait(smem_u32(is_v ? &sh->v_land[st] : &sh->k_land[st]), ph, abort, a.err))
         break;
       widen_tile_fp8(is_v ? sV + st * Lt::kTileBytes : sK + st * Lt::kTileBytes, lane);
+      int lead, tail;
+      if (is_v && v_edges(i, lead, tail)) {
+        __syncwarp();
+        zero_v_rows<D>(sV + st * Lt::kTileBytes, lead, tail, lane);
+      }
       fence_proxy_async();   // generic writes, then the tensor core reads
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(is_v ? &sh->v_full[st] : &sh->k_full[st]));
@@ -679,7 +724,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int g = row % G;
     const bool valid = tok <= tok_last;
     const int pos = casc ? L - 1 : L - qn + (valid ? tok : tok_last);
-    const int ts = (warp & 3) * 32 + lane;        // 0..127 within the warpgroup
     const uint32_t b_sfull = smem_u32(&sh->s_full[t]);
     const uint32_t b_pfull = smem_u32(&sh->p_full[t]), b_pvdone = smem_u32(&sh->pv_done[t]);
     const uint32_t tS = tmem + lane_off + col_s(t), tP = tmem + lane_off + col_p(t);
@@ -836,29 +880,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float ls = (tc::sum_f32x2(acc[0]) + tc::sum_f32x2(acc[1])) +
                        (tc::sum_f32x2(acc[2]) + tc::sum_f32x2(acc[3]));
       l = l * alpha + ls;
-      const int lead = min(kTcKeys, b_lo * kBlock - key0);       // keys not loaded (> 0 only at j == 0)
-      const int tail = (j == n_rel - 1) ? pos_max + 1 - key0 : kTcKeys;  // keys from here on unseen
-      if (lead > 0 || tail < kTcKeys) {
-        // Keys before the first loaded block or past pos_max have P = 0 in
-        // every row, but their V rows may be stale NaN or left over from an
-        // earlier tile: zero them before this warpgroup's P V product may be
-        // issued.  Both warpgroups do it (the MMAs of the two query tiles are
-        // issued in either order); the second writes zeros over zeros.
-        if (!warp_wait(smem_u32(&sh->v_full[j % kVStages]), (j / kVStages) & 1, abort,
-                       a.err)) { done = false; break; }
-        uint8_t* vt = sV + (j % kVStages) * Lt::kTileBytes;
-        const int per_row = Lt::kHalves * 8;
-        const int nlead = lead > 0 ? lead : 0;
-        const int ntail = kTcKeys - tail;
-        for (int e = ts; e < (nlead + ntail) * per_row; e += 128) {
-          const int r = e / per_row;
-          const int key = r < nlead ? r : tail + (r - nlead);
-          const int rem = e % per_row;
-          *reinterpret_cast<uint4*>(vt + (rem >> 3) * Lt::kKvHalf + key * 128 + (rem & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async();
-      }
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
