@@ -291,6 +291,17 @@ int pkv_use_cascade(const pkv_attn_meta *meta, int32_t common_prefix_blocks);
  * device first.  Returns PKV_OK or PKV_E_CUDA. */
 int pkv_get_error(int32_t *error_bits, int clear);
 
+/* TEST HOOK for the timeout path; no counterpart in the pages.  Every on-chip
+ * wait of the kernels gives up after a bounded time (1 s), sets
+ * PKV_ERR_TIMEOUT, lets the CTA's own copies in flight land, frees its tensor
+ * memory and returns.  With enable != 0, the decode and tcgen05 prefill
+ * launches this process makes afterwards (on any device, from any thread)
+ * wait at most 20 us and withhold their first key block or tile, so that
+ * those waits run out and the attention calls return with PKV_ERR_TIMEOUT
+ * set and meaningless output; enable = 0 restores normal launches.  Host
+ * only; never synchronises.  Returns PKV_OK. */
+int pkv_debug_wait_test(int enable);
+
 /* Static, human-readable text for a status code. */
 const char *pkv_status_string(int status);
 

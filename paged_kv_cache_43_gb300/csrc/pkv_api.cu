@@ -848,6 +848,26 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
 }  // namespace
 }  // namespace pkv
 
+namespace pkv {
+namespace {
+// Test hook (pkv_debug_wait_test): 0 = off.
+std::atomic<uint64_t> g_debug_wait_limit_ns{0};
+std::atomic<int32_t> g_debug_stall{0};
+constexpr uint64_t kDebugWaitLimitNs = 20000;   // 20 us
+}  // namespace
+
+void debug_wait_settings(uint64_t* limit_ns, int32_t* stall) {
+  *limit_ns = g_debug_wait_limit_ns.load(std::memory_order_relaxed);
+  *stall = g_debug_stall.load(std::memory_order_relaxed);
+}
+}  // namespace pkv
+
+extern "C" int pkv_debug_wait_test(int enable) {
+  pkv::g_debug_wait_limit_ns.store(enable ? pkv::kDebugWaitLimitNs : 0);
+  pkv::g_debug_stall.store(enable ? 1 : 0);
+  return PKV_OK;
+}
+
 extern "C" int pkv_get_error(int32_t* error_bits, int clear) {
   if (error_bits == nullptr) return PKV_E_NULL;
   int32_t* err;

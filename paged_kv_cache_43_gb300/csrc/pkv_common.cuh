@@ -83,16 +83,25 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitLimitNs and returns false (the caller raises PKV_ERR_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// after `limit_ns` (kWaitLimitNs unless a launch was made with the test hook
+// of pkv_debug_wait_test) and returns false (the caller raises
+// PKV_ERR_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The main-loop wait limit of a launch: kWaitLimitNs, or the short one the
+// test hook of pkv_debug_wait_test sets.
+__device__ __forceinline__ uint64_t wait_limit(uint64_t requested_ns) {
+  return requested_ns != 0 ? requested_ns : kWaitLimitNs;
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32).

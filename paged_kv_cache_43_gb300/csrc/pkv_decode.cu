@@ -157,10 +157,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   const uint64_t policy = policy_evict_first();
   // Issues this warp's block i into stage i % NS (all lanes call; lane 0 acts).
+  // Test hook: warp 0 withholds its first block (no copy, no arrival), so
+  // that its wait for it runs out.
+  const bool withheld = a.debug_stall != 0 && warp == 0;
   auto issue = [&](int i) {
     const int bid = __shfl_sync(0xffffffffu, my_bid, i);
     const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
-    if (lane == 0) {
+    if (lane == 0 && !(withheld && i == 0)) {
       const int st = i % NS;
       const uint32_t dst = wbase_u + st * T::kStageBytes;
       const uint32_t bar = bar0 + 8 * st;
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   for (int i = 0; i < nb_w; ++i) {
     const int st = i % NS;
     const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
-    if (!mbar_wait(bar0 + 8 * st, (i / NS) & 1)) {
+    if (!mbar_wait(bar0 + 8 * st, (i / NS) & 1, wait_limit(a.wait_limit_ns))) {
       timed_out = true;
       break;
     }
@@ -459,6 +462,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     // Let every copy this warp issued land before the CTA's memory is released.
     for (int st = 0; st < NS && st < issued; ++st) {
       const int last = ((issued - 1 - st) / NS) * NS + st;  // last block issued into stage st
+      if (withheld && last == 0) continue;                    // (never issued)
       (void)mbar_wait(bar0 + 8 * st, (last / NS) & 1);
     }
     m[0] = m[1] = -INFINITY;
@@ -628,7 +632,9 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
   const int ngsub = PREFIX ? a.prefix_col_groups : (a.group + 7) / 8;
   dim3 grid(PREFIX ? a.prefix_splits : a.max_splits - a.split_base, a.num_kv_heads * ngsub,
             PREFIX ? 1 : a.num_seqs);
-  kfn<<<grid, kDecodeWarps * 32, smem, stream>>>(kmap, vmap, a);
+  DecodeArgs b = a;
+  debug_wait_settings(&b.wait_limit_ns, &b.debug_stall);
+  kfn<<<grid, kDecodeWarps * 32, smem, stream>>>(kmap, vmap, b);
   return cudaGetLastError();
 }
 

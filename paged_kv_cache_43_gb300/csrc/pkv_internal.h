@@ -60,6 +60,11 @@ struct DecodeArgs {
   int32_t prefix_splits;         // combine: leading split slots that hold prefix partials
   int32_t prefix_len;            // prefix launch: the shared keys [0, prefix_len)
   int32_t prefix_col_groups;     // prefix launch: 8-column groups per kv head
+  // Test hook (pkv_debug_wait_test): main-loop wait limit (0 = the default)
+  // and, when set, warp 0 of every CTA withholds its first block load so
+  // that its wait runs out.
+  uint64_t wait_limit_ns;
+  int32_t debug_stall;
 };
 
 // Varlen causal attention over sequences [seq_begin, seq_begin + num_seqs).
@@ -99,7 +104,16 @@ struct PrefillArgs {
   int32_t max_splits;
   float* ws_o;
   float* ws_lse;
+  // Test hook (pkv_debug_wait_test), tcgen05 kernel: main-loop wait limit (0
+  // = the default) and, when set, the K producer withholds the CTA's first K
+  // tile so that the waits for it run out.
+  uint64_t wait_limit_ns;
+  int32_t debug_stall;
 };
+
+// Settings of the test hook, applied to the decode and tcgen05 prefill
+// launches made after pkv_debug_wait_test (pkv_api.cu).
+void debug_wait_settings(uint64_t* limit_ns, int32_t* stall);
 
 // fp32 I/O: one CTA per (query row, q head), every sequence.
 struct F32Args {

@@ -151,7 +151,8 @@ __device__ __forceinline__ void set_max_regs_dec_other() {
 // or a short time limit passes, so a waiting warp takes no issue slots from
 // the softmax and MMA-issuing warps of its SM sub-partition.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int32_t* abort, int32_t* err) {
+                                              volatile int32_t* abort, int32_t* err,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -159,7 +160,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       raise_error(err, PKV_ERR_TIMEOUT);
       return false;
@@ -170,10 +171,10 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 // Warp-uniform version: lane 0 waits, the verdict is broadcast, and the other
 // lanes then observe the (already completed) phase themselves.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort,
-                                          int32_t* err) {
+                                          int32_t* err, uint64_t limit_ns) {
   const int lane = threadIdx.x & 31;
   bool ok = true;
-  if (lane == 0) ok = wait_or_abort(bar, parity, abort, err);
+  if (lane == 0) ok = wait_or_abort(bar, parity, abort, err, limit_ns);
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   if (ok && lane != 0) ok = mbar_test(bar, parity);   // completed: observe it
   return __all_sync(0xffffffffu, ok);
@@ -446,6 +447,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
   volatile int32_t* abort = &sh->abort;
+  const uint64_t wlim = wait_limit(a.wait_limit_ns);
   TC_MARK(0);
 #ifdef PKV_TC_TIMELINE
   const int cta_lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
@@ -558,10 +560,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     };
     int g_prev = -1, g_cur = load_ids4(0), g_nxt = load_ids4(1);
+    // Test hook: the K producer withholds the first K tile (no copy, no
+    // arrival), so that the waits for it run out.
+    const bool withhold_k0 = a.debug_stall != 0;
+    // Before the CTA's shared memory is released, every copy a producer
+    // started must have landed: after its loop (normal or given up) it waits,
+    // with the full limit, for the last tile of each ring stage it filled
+    // (earlier ones were consumed before the stage was refilled).
+    auto drain = [&](int n_issued, int stages, bool is_v, bool land) {
+      for (int r = max(0, n_issued - stages); r < n_issued; ++r) {
+        if (!is_v && r == 0 && withhold_k0) continue;
+        const int st = r % stages;
+        const uint32_t bar = smem_u32(land ? (is_v ? &sh->v_land[st] : &sh->k_land[st])
+                                           : (is_v ? &sh->v_full[st] : &sh->k_full[st]));
+        if (lane == 0) (void)mbar_wait(bar, (r / stages) & 1);
+      }
+      __syncwarp();
+    };
     if constexpr (!FP8) {
       const bool is_v = warp == 10;
       const int stages = is_v ? kVStages : kKStages;
       uint32_t land_phase = 0;   // parity of each stage's next v_land phase
+      int n_issued = 0, pending_land = -1;
       for (int rel = 0; rel < n_rel; ++rel) {
         if (rel > 0 && (rel & 3) == 0) {
           g_cur = g_nxt;
@@ -570,17 +590,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int st = rel % stages;
         if (rel >= stages &&
             !warp_wait(smem_u32(is_v ? &sh->v_empty[st] : &sh->k_empty[st]),
-                       ((rel / stages) - 1) & 1, abort, a.err))
+                       ((rel / stages) - 1) & 1, abort, a.err, wlim))
           break;
         int lead, tail;
         const bool edge = is_v && v_edges(rel, lead, tail);
-        issue_tile(j0 + rel, g_cur, rel & 3, is_v,
-                   smem_u32((is_v ? sV : sK) + st * Lt::kTileBytes),
-                   smem_u32(edge ? &sh->v_land[st] : is_v ? &sh->v_full[st] : &sh->k_full[st]));
+        if (!(!is_v && rel == 0 && withhold_k0))
+          issue_tile(j0 + rel, g_cur, rel & 3, is_v,
+                     smem_u32((is_v ? sV : sK) + st * Lt::kTileBytes),
+                     smem_u32(edge ? &sh->v_land[st] : is_v ? &sh->v_full[st] : &sh->k_full[st]));
+        n_issued = rel + 1;
         if (lane == 0) TC_MARK((is_v ? 200 : 100) + (rel & 63));
         if (edge) {   // landed, edge rows zeroed, then full
-          if (!warp_wait(smem_u32(&sh->v_land[st]), (land_phase >> st) & 1u, abort, a.err))
+          pending_land = st;
+          if (!warp_wait(smem_u32(&sh->v_land[st]), (land_phase >> st) & 1u, abort, a.err, wlim))
             break;
+          pending_land = -1;
           land_phase ^= 1u << st;
           zero_v_rows<D>(sV + st * Lt::kTileBytes, lead, tail, lane);
           fence_proxy_async();   // generic writes, then the tensor core reads
@@ -588,7 +612,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) mbar_arrive(smem_u32(&sh->v_full[st]));
         }
       }
+      // An edge tile whose landing wait gave up is still in flight on v_land;
+      // the other tiles' copies complete on their full barriers.
+      if (pending_land >= 0 && lane == 0)
+        (void)mbar_wait(smem_u32(&sh->v_land[pending_land]), (land_phase >> pending_land) & 1u);
+      drain(pending_land >= 0 ? n_issued - 1 : n_issued, stages, is_v, false);
     } else {
+      int k_issued = 0, v_issued = 0;
       for (int rel = 0; rel <= n_rel; ++rel) {
         if (rel > 0 && (rel & 3) == 0) {
           g_prev = g_cur;
@@ -598,25 +628,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (rel < n_rel) {
           const int st = rel % kKStages;
           if (rel >= kKStages &&
-              !warp_wait(smem_u32(&sh->k_empty[st]), ((rel / kKStages) - 1) & 1, abort, a.err))
+              !warp_wait(smem_u32(&sh->k_empty[st]), ((rel / kKStages) - 1) & 1, abort, a.err, wlim))
             break;
           // (the codes land on k_land; warp 10 widens them, then k_full)
-          issue_tile(j0 + rel, g_cur, rel & 3, false, smem_u32(sK + st * Lt::kTileBytes),
-                     smem_u32(&sh->k_land[st]));
+          if (!(rel == 0 && withhold_k0))
+            issue_tile(j0 + rel, g_cur, rel & 3, false, smem_u32(sK + st * Lt::kTileBytes),
+                       smem_u32(&sh->k_land[st]));
+          k_issued = rel + 1;
           if (lane == 0) TC_MARK(100 + (rel & 63));
         }
         if (rel >= 1) {
           const int rv = rel - 1;   // ring position of the V tile
           const int st = rv % kVStages;
           if (rv >= kVStages &&
-              !warp_wait(smem_u32(&sh->v_empty[st]), ((rv / kVStages) - 1) & 1, abort, a.err))
+              !warp_wait(smem_u32(&sh->v_empty[st]), ((rv / kVStages) - 1) & 1, abort, a.err, wlim))
             break;
           issue_tile(j0 + rv, (rv >> 2) == (rel >> 2) ? g_cur : g_prev, rv & 3, true,
                      smem_u32(sV + st * Lt::kTileBytes), smem_u32(&sh->v_land[st]));
+          v_issued = rv + 1;
           if (lane == 0) TC_MARK(200 + (rv & 63));
         }
       }
+      drain(k_issued, kKStages, false, true);
+      drain(v_issued, kVStages, true, true);
     }
+    if (warp == 8 && lane == 0) (void)mbar_wait(q_full, 0);   // the query tiles too
+    __syncwarp();
    } else if (warp == 9 && !kSelfIssue) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
@@ -628,7 +665,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int s_next[kTcTiles] = {0, 0};   // next tile index whose S is issued
         int pv_next[kTcTiles] = {0, 0};  // next tile index whose P V is issued
         int k_released = 0, v_released = 0;  // ring stages handed back to the producer
-        bool ok = wait_or_abort(q_ready, 0, abort, a.err);
+        bool ok = wait_or_abort(q_ready, 0, abort, a.err, wlim);
         uint64_t idle_since = 0;
         while (ok) {
           bool progress = false;
@@ -681,7 +718,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               idle_since = now;
             } else if (*abort) {
               ok = false;
-            } else if (now - idle_since > kWaitLimitNs) {
+            } else if (now - idle_since > wlim) {
               *abort = 1;
               raise_error(a.err, PKV_ERR_TIMEOUT);
               ok = false;
@@ -700,7 +737,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < n_rel; ++i) {
       const int st = is_v ? i % kVStages : i % kKStages;
       const int ph = is_v ? (i / kVStages) & 1 : (i / kKStages) & 1;
-      if (!warp_wait(smem_u32(is_v ? &sh->v_land[st] : &sh->k_land[st]), ph, abort, a.err))
+      if (!warp_wait(smem_u32(is_v ? &sh->v_land[st] : &sh->k_land[st]), ph, abort, a.err, wlim))
         break;
       widen_tile_fp8(is_v ? sV + st * Lt::kTileBytes : sK + st * Lt::kTileBytes, lane);
       int lead, tail;
@@ -736,7 +773,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int ds = casc ? (valid ? tok : tok_last) : s;
       sl2 *= __ldg(a.k_descale + static_cast<int64_t>(ds) * a.num_kv_heads + kvh);
       out_scale = __ldg(a.v_descale + static_cast<int64_t>(ds) * a.num_kv_heads + kvh);
-      bool qok = warp_wait(q_full, 0, abort, a.err);
+      bool qok = warp_wait(q_full, 0, abort, a.err, wlim);
       if (qok) {
         uint8_t* qrow = sQ + t * Lt::kQTile + row * 128;
         uint4 v[2 * 8];
@@ -792,9 +829,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t my_issued = smem_u32(&sh->issued[t]);
     const uint32_t other_issued = smem_u32(&sh->issued[t ^ 1]);
     if (issuer) {
-      if (wait_or_abort(q_ready, 0, abort, a.err) &&
-          wait_or_abort(smem_u32(&sh->k_full[0]), 0, abort, a.err) &&
-          (t == 0 || wait_or_abort(other_issued, 0, abort, a.err))) {
+      if (wait_or_abort(q_ready, 0, abort, a.err, wlim) &&
+          wait_or_abort(smem_u32(&sh->k_full[0]), 0, abort, a.err, wlim) &&
+          (t == 0 || wait_or_abort(other_issued, 0, abort, a.err, wlim))) {
         tc::fence_after_sync();
         TC_MARK(300 + 64 * t);
         issue_s(t, 0);
@@ -805,7 +842,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
     for (int j = 0; done && j < n_rel; ++j) {
       // S_t(j) complete (its commit also covers P_t(j - 1) V, so O_t is stable)
-      if (!warp_wait(b_sfull, j & 1, abort, a.err)) { done = false; break; }
+      if (!warp_wait(b_sfull, j & 1, abort, a.err, wlim)) { done = false; break; }
       tc::fence_after_sync();
       if (quarter == 0 && lane == 0) TC_MARK(700 + 64 * t + (j & 63));
       float x[kTcKeys];
@@ -889,17 +926,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // (a failed wait leaves the other warps to give up on s_full)
         // this tile's group j: after the other tile's group j - 1 (tile 0)
         // or group j (tile 1), i.e. the other barrier's phase j or j + 1
-        if (wait_or_abort(b_pfull, j & 1, abort, a.err) &&
+        if (wait_or_abort(b_pfull, j & 1, abort, a.err, wlim) &&
             wait_or_abort(smem_u32(&sh->v_full[j % kVStages]), (j / kVStages) & 1, abort,
-                          a.err) &&
-            (!paired || wait_or_abort(other_issued, (j + t) & 1, abort, a.err))) {
+                          a.err, wlim) &&
+            (!paired || wait_or_abort(other_issued, (j + t) & 1, abort, a.err, wlim))) {
           tc::fence_after_sync();
           TC_MARK(500 + 64 * t + (j & 63));
           issue_pv(t, j);
           tc::commit(smem_u32(&sh->v_empty[j % kVStages]));
           const int jn = j + 1;
           if (jn < n_rel && wait_or_abort(smem_u32(&sh->k_full[jn % kKStages]),
-                                          (jn / kKStages) & 1, abort, a.err)) {
+                                          (jn / kKStages) & 1, abort, a.err, wlim)) {
             tc::fence_after_sync();
             TC_MARK(300 + 64 * t + (jn & 63));
             issue_s(t, jn);
@@ -915,7 +952,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (void)mbar_wait(drain, 0);
     }
     __syncwarp();
-    if (done && casc && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
+    if (done && casc && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim)) {
       // cascade prefix: the row's normalised partial and log2-sum-exp (in the
       // scaled log2 domain of m_used) for the merge
       tc::fence_after_sync();
@@ -937,7 +974,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (valid) a.ws_lse[wrow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
-    } else if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err)) {
+    } else if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim)) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? out_scale / l : 0.f;
       __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * D;
@@ -998,7 +1035,9 @@ cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const 
                                         (a.prefix_tiles * kTcKeys)
                                   : a.num_seqs;
   dim3 grid(a.num_mtiles, a.num_kv_heads, gz);
-  kfn<<<grid, kTcThreads, smem, stream>>>(qmap, kmap, vmap, a);
+  PrefillArgs b = a;
+  debug_wait_settings(&b.wait_limit_ns, &b.debug_stall);
+  kfn<<<grid, kTcThreads, smem, stream>>>(qmap, kmap, vmap, b);
   return cudaGetLastError();
 }
 

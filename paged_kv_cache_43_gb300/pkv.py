@@ -30,7 +30,7 @@ EXPORTED = ("pkv_write", "pkv_write_fp8", "pkv_attention_workspace_size", "pkv_a
             "pkv_attention_cascade_workspace_size", "pkv_attention_cascade",
             "pkv_attention_cascade_fp8", "pkv_use_cascade",
             "pkv_get_error", "pkv_status_string", "pkv_last_cuda_error",
-            "pkv_last_cuda_error_string")
+            "pkv_last_cuda_error_string", "pkv_debug_wait_test")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -110,6 +110,8 @@ def load(path: str | None = None):
         lib.pkv_last_cuda_error.argtypes = []
         lib.pkv_last_cuda_error_string.restype = ctypes.c_char_p
         lib.pkv_last_cuda_error_string.argtypes = []
+        lib.pkv_debug_wait_test.restype = ctypes.c_int
+        lib.pkv_debug_wait_test.argtypes = [ctypes.c_int]
         _lib = lib
         return lib
 
@@ -384,6 +386,13 @@ def get_error(clear: bool = True) -> int:
     bits = ctypes.c_int32(0)
     _check(load().pkv_get_error(ctypes.byref(bits), int(clear)))
     return int(bits.value)
+
+
+def debug_wait_test(enable: bool) -> None:
+    """Test hook of the timeout path (pkv_debug_wait_test): while enabled,
+    decode and tcgen05 prefill launches wait at most 20 us and withhold their
+    first key block, so their waits run out and PKV_ERR_TIMEOUT is set."""
+    _check(load().pkv_debug_wait_test(1 if enable else 0))
 
 
 def status_string(status: int) -> str:
