@@ -824,7 +824,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // its S(0) being phase 0; a turn waits for the other tile's previous
     // group, which cannot run two phases ahead of the waiter.
     constexpr bool self_issue = kSelfIssue;
-    const bool issuer = self_issue && done && quarter == 0 && lane == 0;
+    // (tile t's issuer sits on SM sub-partition t, apart from the other tile's)
+    const bool issuer = self_issue && done && quarter == t && lane == 0;
     const bool paired = ntq > 1;
     const uint32_t my_issued = smem_u32(&sh->issued[t]);
     const uint32_t other_issued = smem_u32(&sh->issued[t ^ 1]);
