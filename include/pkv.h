@@ -268,8 +268,8 @@ int pkv_attention_cascade(void *out, const void *q, const void *k_cache, const v
 /* Cascade attention over e4m3 caches: as pkv_attention_cascade with the
  * descales of pkv_attention_fp8 (fp32 [num_seqs, num_kv_heads], device; each
  * row uses its own sequence's descales, the shared keys included).  The shared
- * keys run on the tcgen05 kernel, so head_size must be 128 and the group size
- * divide 128 (PKV_E_SHAPE otherwise); workspace size from
+ * keys run on the tcgen05 kernel, so the group size must divide 128
+ * (PKV_E_SHAPE otherwise); workspace size from
  * pkv_attention_cascade_workspace_size with the e4m3 cache descriptor. */
 int pkv_attention_cascade_fp8(void *out, const void *q, const void *k_cache,
                               const void *v_cache, const int32_t *block_tables,

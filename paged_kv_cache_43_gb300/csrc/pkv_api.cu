@@ -359,8 +359,7 @@ int make_cascade_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int32_t p
   const int G = m->num_q_heads / c->num_kv_heads;
   p->col_groups = static_cast<int>((static_cast<int64_t>(m->num_seqs) * G + 7) / 8);
   // e4m3 caches: the shared keys only on the widening tcgen05 kernel
-  if (c->dtype == PKV_FP8_E4M3 && !(c->head_size == 128 && prefill_tc_supported(128, G)))
-    return PKV_E_SHAPE;
+  if (c->dtype == PKV_FP8_E4M3 && !prefill_tc_supported(c->head_size, G)) return PKV_E_SHAPE;
   if (prefill_tc_supported(c->head_size, G)) {
     // tcgen05: all decode rows of a kv head in 128-row tiles, at least two
     // 128-key tiles per CTA, about half the SMs (their partials are merged)
@@ -620,7 +619,7 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
     f.v_descale = v_descale;
     f.scale_log2 = scale * LOG2E;
     f.longest_first = p.num_decode == 0 ? 1 : 0;   // alone on the GPU, or beside decode
-    if (prefill_tc_supported(cache->head_size, G) && (!fp8 || cache->head_size == 128)) {
+    if (prefill_tc_supported(cache->head_size, G)) {
       // tcgen05/TMEM kernel: two tiles of 128/G tokens x G heads per CTA.
       const int toks = prefill_tc_tokens_per_cta(G);
       f.num_mtiles = (meta->max_query_len + toks - 1) / toks;
@@ -630,8 +629,8 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
         return e;
       PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, st));
     } else {
-      // FP8 caches, and group sizes that do not divide 128 rows: mma.sync
-      // kernel, 64 rows per CTA.
+      // group sizes that do not divide 128 rows: mma.sync kernel, 64 rows per
+      // CTA.
       const int64_t rows = static_cast<int64_t>(meta->max_query_len) * G;
       f.num_mtiles = static_cast<int32_t>((rows + kPrefillRows - 1) / kPrefillRows);
       PKV_TRY(launch_prefill_bf16(kmap, vmap, f, cache->head_size, fp8, st));

@@ -38,11 +38,11 @@
 //    holds the short ones; beside a decode launch the plain order stays.
 //  * every wait is an mbarrier with a bounded spin and a CTA-wide abort flag;
 //    TMEM is freed on every path.
-//  * FP8 (e4m3) cache, head_size 128: TMA lands each tile's codes (128 keys x
-//    128 B, 128-byte swizzle) in the first half of its ring slot and warp 10
-//    (K) or 11 (V) widens them in place to fp16 in the bf16 tiles' layout
-//    (e4m3 is exact in fp16; a row's codes are read before its first fp16 half
-//    overwrites them), then marks the slot full for the MMAs;
+//  * FP8 (e4m3) cache: TMA lands each tile's codes (128 keys x D bytes, the
+//    128- or 64-byte swizzle of the row width) in the first part of its ring
+//    slot and warp 10 (K) or 11 (V) widens them in place to fp16 in the bf16
+//    tiles' layout (e4m3 is exact in fp16; codes are read before the fp16
+//    rows written over them), then marks the slot full for the MMAs;
 //    each softmax thread converts its own Q row to fp16 (a row beyond 2^14
 //    scaled by 2^-e, its scores by 2^e) and the MMAs run on fp16 operands with
 //    P in fp16.  The K descale folds into the score scale, the V descale into
@@ -243,6 +243,42 @@ __device__ __forceinline__ void zero_v_rows(uint8_t* vt, int lead, int tail, int
   }
 }
 
+// head_size 64: the tile's 128 code rows of 64 B (64-byte swizzle: chunk c of
+// row r at r * 64 + ((c ^ (r / 2 % 4)) << 4)) land in its first 8 KB and
+// widen into 128 fp16 rows of 128 B (128-byte swizzle).  Batch b (rows 16b ..
+// 16b + 15) writes bytes [2048 b, 2048 b + 2048), the codes of batches 2b and
+// 2b + 1; going from the last batch to the first, those were read earlier
+// (or, for b = 0, by this batch before its writes).  A lane reads two 16-code
+// chunks per batch.
+__device__ __forceinline__ void widen_tile_fp8_d64(uint8_t* tile, int lane) {
+  const int c = lane & 3;           // code chunk: columns 16c .. 16c + 15
+#pragma unroll 1
+  for (int b = kTcKeys / 16 - 1; b >= 0; --b) {
+    uint4 codes[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = 16 * b + 8 * i + (lane >> 2);
+      codes[i] = *reinterpret_cast<const uint4*>(tile + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+    }
+    uint4 lo[2], hi[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint2 x = e4m3x4_to_f16x4(codes[i].x), y = e4m3x4_to_f16x4(codes[i].y);
+      const uint2 z = e4m3x4_to_f16x4(codes[i].z), w = e4m3x4_to_f16x4(codes[i].w);
+      lo[i] = make_uint4(x.x, x.y, y.x, y.y);
+      hi[i] = make_uint4(z.x, z.y, w.x, w.y);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = 16 * b + 8 * i + (lane >> 2);
+      *reinterpret_cast<uint4*>(tile + r * 128 + (((2 * c) ^ (r & 7)) << 4)) = lo[i];
+      *reinterpret_cast<uint4*>(tile + r * 128 + (((2 * c + 1) ^ (r & 7)) << 4)) = hi[i];
+    }
+    __syncwarp();
+  }
+}
+
 // Which (sequence, row-tile pair, kv head) this CTA computes.  The block
 // scheduler starts CTAs in launch order, so with `longest_first` the grid is
 // handed out longest first (list scheduling): the units (sequence, pair) are
@@ -315,7 +351,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
-  static_assert(!FP8 || D == 128, "the e4m3 path widens 128-byte code rows");
   using Lt = TcLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -536,7 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool in_range = blk < nblk && blk >= b_lo;
         ok[b] = in_range && bid[b] >= 0 && bid[b] < a.num_blocks;
         if (!is_v && in_range && !ok[b] && lane == 0) raise_error(a.err, PKV_ERR_BLOCK_ID);
-        bytes += ok[b] ? (FP8 ? 2048u : Lt::kHalves * 2048u) : 0u;
+        bytes += ok[b] ? (FP8 ? 16u * D : Lt::kHalves * 2048u) : 0u;
       }
       if (lane == 0) {
         if (bytes == 0) {
@@ -546,8 +581,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int b = 0; b < kBlocks; ++b) {
             if (!ok[b]) continue;
-            if constexpr (FP8) {  // 16 rows x 128 codes: rows b*16 .. b*16+15 of the tile
-              tma_load_3d(dst + b * 2048, is_v ? &vmap : &kmap, full, 0, kvh, bid[b] * kBlock,
+            if constexpr (FP8) {  // 16 rows x D codes: rows b*16 .. b*16+15 of the tile
+              tma_load_3d(dst + b * 16 * D, is_v ? &vmap : &kmap, full, 0, kvh, bid[b] * kBlock,
                           keep);
             } else {
 #pragma unroll
@@ -739,7 +774,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int ph = is_v ? (i / kVStages) & 1 : (i / kKStages) & 1;
       if (!warp_wait(smem_u32(is_v ? &sh->v_land[st] : &sh->k_land[st]), ph, abort, a.err, wlim))
         break;
-      widen_tile_fp8(is_v ? sV + st * Lt::kTileBytes : sK + st * Lt::kTileBytes, lane);
+      if constexpr (D == 128)
+        widen_tile_fp8(is_v ? sV + st * Lt::kTileBytes : sK + st * Lt::kTileBytes, lane);
+      else
+        widen_tile_fp8_d64(is_v ? sV + st * Lt::kTileBytes : sK + st * Lt::kTileBytes, lane);
       int lead, tail;
       if (is_v && v_edges(i, lead, tail)) {
         __syncwarp();
@@ -779,7 +817,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint4 v[2 * 8];
         float amax = 0.f;
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < Lt::kHalves; ++h)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             v[h * 8 + j] = *reinterpret_cast<const uint4*>(qrow + h * Lt::kQHalf + ((j ^ (row & 7)) << 4));
@@ -792,7 +830,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float down = pow2f(-ex);
         sl2 *= pow2f(ex);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < Lt::kHalves; ++h)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint4 u = v[h * 8 + j];
@@ -1056,7 +1094,9 @@ cudaError_t launch_prefill_tc(const CUtensorMap& qmap, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const PrefillArgs& a, int head_size,
                               bool fp8, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_mtiles == 0) return cudaSuccess;
-  if (fp8) return launch_tc_t<128, true>(qmap, kmap, vmap, a, stream);
+  if (fp8)
+    return head_size == 128 ? launch_tc_t<128, true>(qmap, kmap, vmap, a, stream)
+                            : launch_tc_t<64, true>(qmap, kmap, vmap, a, stream);
   if (head_size == 128) return launch_tc_t<128, false>(qmap, kmap, vmap, a, stream);
   return launch_tc_t<64, false>(qmap, kmap, vmap, a, stream);
 }

@@ -173,13 +173,15 @@ def test_cascade_captured_in_a_cuda_graph_replays_correctly():
 
 # ------------------------------------------------------------ e4m3 caches
 
-@pytest.mark.parametrize("S,hq,hkv,pblocks", [(8, 8, 8, 1), (16, 32, 8, 5), (40, 8, 2, 64),
-                                              (200, 32, 8, 5), (3, 64, 8, 16)])
-def test_cascade_fp8_matches_oracle(S, hq, hkv, pblocks):
+@pytest.mark.parametrize("S,hq,hkv,pblocks,d", [(8, 8, 8, 1, 128), (16, 32, 8, 5, 128),
+                                                (40, 8, 2, 64, 128), (200, 32, 8, 5, 128),
+                                                (3, 64, 8, 16, 128), (8, 8, 8, 1, 64),
+                                                (16, 32, 8, 5, 64), (40, 8, 2, 64, 64)])
+def test_cascade_fp8_matches_oracle(S, hq, hkv, pblocks, d):
     """Descales drawn per (sequence, kv head): every row, the shared keys
-    included, must use its own sequence's."""
+    included, must use its own sequence's.  head_size 64 and 128."""
     from tests.support import fp8_scale_tensors, gpu_fp8_caches, oracle_step_fp8
-    wl = _shared(S, pblocks, hq, hkv, 128, 2, pblocks * 16 + 700, seed=S + pblocks)
+    wl = _shared(S, pblocks, hq, hkv, d, 2, pblocks * 16 + 700, seed=S + pblocks + d)
     g = wl.to("cuda")
     ks, vs, _, _ = fp8_scale_tensors(hkv, S, 13)
     rng = np.random.default_rng(S * 3 + pblocks)
@@ -200,7 +202,7 @@ def test_cascade_fp8_matches_oracle(S, hq, hkv, pblocks):
 
 def test_cascade_fp8_shapes_without_the_tcgen05_prefix_are_refused():
     lib = pkv.load()
-    for hq, hkv, d in ((8, 8, 64), (12, 4, 128)):          # head_size 64; group 3
+    for hq, hkv, d in ((12, 4, 128), (12, 4, 64)):          # group 3
         wl = _shared(8, 4, hq, hkv, d, 100, 300, seed=2)
         g = wl.to("cuda")
         kc8 = torch.zeros(g.k_cache.shape, dtype=torch.uint8, device="cuda")
