@@ -240,21 +240,25 @@ int pkv_attention_fp8(void *out, const void *q, const void *k_cache, const void 
                       void *stream);
 
 /* Cascade attention ([book] ch. 6: "Structure des métadonnées", the cascade
- * fields use_cascade / common_prefix_len; the sequence diagram, where the
- * cascade branch runs a prefix call and a suffix call and merges them with
- * merge_attn_states; "Réflexion de conception", the use_cascade_attention
- * gate).  For a decode batch (every sequence one query row, max_query_len <=
- * 1, no sliding window) whose sequences' first common_prefix_blocks
- * block-table entries name the same physical blocks (the caller guarantees
- * it; sequence 0's entries are read): the shared prefix keys are attended
- * once for all rows of all sequences (K/V read once per 8 (sequence, q head)
- * columns instead of once per sequence), each row's own keys after the prefix
- * separately, and the partial results merged.  Same result as pkv_attention
- * (arguments as there).  Every sequence needs L > 16 * common_prefix_blocks
- * (else its rows are zeroed and PKV_ERR_CONTEXT_LEN set).  bf16 caches only
- * (PKV_E_DTYPE otherwise); PKV_E_META for prefill rows, a window, or a prefix
- * outside [1, min(block_table_stride, (max_context_len - 1) / 16)].  The
- * workspace is required (size from the function below).  e4m3 caches:
+ * fields use_cascade / common_prefix_len / cu_prefix_query_lens; the sequence
+ * diagram, where the cascade branch runs a prefix call over every query token
+ * and a suffix call and merges them with merge_attn_states; "Réflexion de
+ * conception", the use_cascade_attention gate).  For a batch -- decode rows,
+ * or meta->num_decode_seqs decode sequences followed by chunked-prefill
+ * sequences -- whose sequences' first common_prefix_blocks block-table entries
+ * name the same physical blocks (the caller guarantees it; sequence 0's
+ * entries are read): the shared prefix keys are attended once for all query
+ * rows (K/V read once per 128-row tile of rows instead of once per sequence),
+ * each row's own keys after the prefix separately (causally inside a chunk),
+ * and the partial results merged.  Same result as pkv_attention (arguments as
+ * there).  Every query row must sit after the prefix: L - q_len >=
+ * 16 * common_prefix_blocks for a chunk, L > 16 * common_prefix_blocks for a
+ * decode row (else the sequence's rows are zeroed and PKV_ERR_CONTEXT_LEN
+ * set).  With chunk rows the group size must divide 128 (PKV_E_SHAPE) and
+ * num_decode_seqs be given (>= 0, PKV_E_META otherwise).  bf16 caches only
+ * (PKV_E_DTYPE otherwise); PKV_E_META for a window, or a prefix outside
+ * [1, min(block_table_stride, (max_context_len - 1) / 16)].  The workspace
+ * is required (size from the function below).  e4m3 caches:
  * pkv_attention_cascade_fp8 (PKV_E_DTYPE here). */
 size_t pkv_attention_cascade_workspace_size(const pkv_cache_desc *cache,
                                             const pkv_attn_meta *meta,

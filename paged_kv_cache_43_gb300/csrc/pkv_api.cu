@@ -337,6 +337,8 @@ struct CascadePlan {
   int prefix_blocks = 0;
   int prefix_split_blocks = 0;
   int prefix_splits = 0;
+  int num_decode = 0;        // leading decode sequences (one query row each)
+  int rows = 0;              // query rows of the prefix launch (tokens)
   int col_groups = 0;        // 8-column groups of (sequence, q head in group) per kv head
   int split_blocks = 0;      // suffix split size
   int max_splits = 0;        // prefix_splits + the longest suffix's splits
@@ -349,14 +351,21 @@ int make_cascade_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int32_t p
   if (int st = check_cache(c)) return st;
   if (c->dtype != PKV_BF16 && c->dtype != PKV_FP8_E4M3) return PKV_E_DTYPE;
   if (int st = check_meta(c, m)) return st;
-  // decode rows only, no window, and a prefix that every query follows
-  if (m->max_query_len > 1 || m->sliding_window != 0 || prefix_blocks < 1 ||
-      prefix_blocks > m->block_table_stride ||
-      static_cast<int64_t>(prefix_blocks) * kBlock >= m->max_context_len)
+  // no window, and a prefix that every query follows; chunked-prefill rows
+  // after num_decode_seqs decode sequences
+  const bool chunks = m->max_query_len > 1;
+  if (m->sliding_window != 0 || prefix_blocks < 1 || prefix_blocks > m->block_table_stride ||
+      static_cast<int64_t>(prefix_blocks) * kBlock >= m->max_context_len ||
+      (chunks && (m->num_decode_seqs < 0 || m->num_decode_seqs > m->num_seqs)))
     return PKV_E_META;
   *p = CascadePlan{};
   p->prefix_blocks = prefix_blocks;
   const int G = m->num_q_heads / c->num_kv_heads;
+  // chunk rows: the shared keys and each chunk's own keys both on the tcgen05
+  // kernel (group sizes dividing 128)
+  if (chunks && !prefill_tc_supported(c->head_size, G)) return PKV_E_SHAPE;
+  p->num_decode = chunks ? m->num_decode_seqs : m->num_seqs;
+  p->rows = chunks ? m->num_tokens : m->num_seqs;
   p->col_groups = static_cast<int>((static_cast<int64_t>(m->num_seqs) * G + 7) / 8);
   // e4m3 caches: the shared keys only on the widening tcgen05 kernel
   if (c->dtype == PKV_FP8_E4M3 && !prefill_tc_supported(c->head_size, G)) return PKV_E_SHAPE;
@@ -365,7 +374,7 @@ int make_cascade_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int32_t p
     // 128-key tiles per CTA, about half the SMs (their partials are merged)
     p->tc_prefix = true;
     const int per_cta = prefill_tc_tokens_per_cta(G);
-    p->prefix_mtiles = (m->num_seqs + per_cta - 1) / per_cta;
+    p->prefix_mtiles = (p->rows + per_cta - 1) / per_cta;
     const int ktiles = (prefix_blocks * kBlock + 127) / 128;
     const int64_t units = static_cast<int64_t>(p->prefix_mtiles) * c->num_kv_heads;
     int tiles = static_cast<int>((ktiles * units + num_sms / 2 - 1) / (num_sms / 2));
@@ -383,11 +392,12 @@ int make_cascade_plan(const pkv_cache_desc* c, const pkv_attn_meta* m, int32_t p
   }
   const int suffix_blocks = (m->max_context_len + kBlock - 1) / kBlock - prefix_blocks;
   const int g_sub = (G + 7) / 8;
-  p->split_blocks =
-      choose_split_blocks(suffix_blocks, static_cast<int64_t>(m->num_seqs) * c->num_kv_heads * g_sub,
-                          num_sms, m->kv_split_tokens);
+  p->split_blocks = choose_split_blocks(
+      suffix_blocks, static_cast<int64_t>(std::max(p->num_decode, 1)) * c->num_kv_heads * g_sub,
+      num_sms, m->kv_split_tokens);
+  // decode rows: the longest suffix's splits; chunk rows: one suffix partial
   p->max_splits = p->prefix_splits + (suffix_blocks + p->split_blocks - 1) / p->split_blocks;
-  const size_t rows = static_cast<size_t>(m->num_seqs) * m->num_q_heads * p->max_splits;
+  const size_t rows = static_cast<size_t>(p->rows) * m->num_q_heads * p->max_splits;
   p->ws_o_bytes = round_up(rows * c->head_size * sizeof(float), 256);
   p->ws_bytes = p->ws_o_bytes + round_up(rows * sizeof(float), 256);
   return PKV_OK;
@@ -804,7 +814,8 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
     f.query_start_loc = query_start_loc;
     f.err = err;
     f.bt_stride = meta->block_table_stride;
-    f.num_seqs = meta->num_seqs;
+    f.num_seqs = p.rows;              // the prefix launch's rows: query tokens
+    f.casc_seqs = meta->num_seqs;
     f.num_q_heads = meta->num_q_heads;
     f.num_kv_heads = cache->num_kv_heads;
     f.group = d.group;
@@ -833,14 +844,60 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
     pa.prefix_col_groups = p.col_groups;
     PKV_TRY(launch_cascade_prefix_bf16(kmap, vmap, pa, cache->head_size, pst));
   }
-  // suffix: each row against its own keys after the prefix; then the merge
+  // suffix: each row against its own keys after the prefix (decode rows on
+  // the split-K decode kernel, chunk rows causally on the tcgen05 kernel);
+  // then the merges
   DecodeArgs sa = d;
+  sa.num_seqs = p.num_decode;
   sa.split_blocks = p.split_blocks;
   sa.key_begin_blocks = p.prefix_blocks;
   sa.split_base = p.prefix_splits;
   PKV_TRY(launch_decode_bf16(kmap, vmap, sa, cache->head_size, fp8, st));
+  const int npf = meta->num_seqs - p.num_decode;
+  if (npf > 0) {
+    PrefillArgs f{};
+    f.out = out;
+    f.q = q;
+    f.block_tables = block_tables;
+    f.context_lens = context_lens;
+    f.query_start_loc = query_start_loc;
+    f.err = err;
+    f.bt_stride = meta->block_table_stride;
+    f.seq_begin = p.num_decode;
+    f.num_seqs = npf;
+    f.num_q_heads = meta->num_q_heads;
+    f.num_kv_heads = cache->num_kv_heads;
+    f.group = d.group;
+    f.num_blocks = cache->num_blocks;
+    f.num_tokens = meta->num_tokens;
+    f.max_query_len = meta->max_query_len;
+    f.k_descale = k_descale;
+    f.v_descale = v_descale;
+    f.scale_log2 = d.scale_log2;
+    const int toks = prefill_tc_tokens_per_cta(d.group);
+    f.num_mtiles = (meta->max_query_len + toks - 1) / toks;
+    f.key_begin = p.prefix_blocks * kBlock;
+    f.split_base = p.prefix_splits;
+    f.max_splits = p.max_splits;
+    f.ws_o = d.ws_o;
+    f.ws_lse = d.ws_lse;
+    CUtensorMap qmap;
+    if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
+                                 cache->head_size, d.group))
+      return e;
+    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, st));
+  }
   if (int e = fork.join()) return e;
   PKV_TRY(launch_combine_bf16(sa, cache->head_size, st));
+  if (npf > 0) {
+    // chunk rows are the query tokens after the decode rows
+    DecodeArgs mr = sa;
+    mr.merge_rows_begin = p.num_decode;
+    mr.merge_rows_end = meta->num_tokens;
+    mr.num_seqs = meta->num_tokens - p.num_decode;
+    mr.casc_seqs = meta->num_seqs;
+    PKV_TRY(launch_combine_bf16(mr, cache->head_size, st));
+  }
   return PKV_OK;
 }
 

@@ -104,6 +104,18 @@ __device__ __forceinline__ uint64_t wait_limit(uint64_t requested_ns) {
   return requested_ns != 0 ? requested_ns : kWaitLimitNs;
 }
 
+// The sequence holding query row `tok`: the s with qsl[s] <= tok < qsl[s + 1]
+// (binary search over the num_seqs + 1 ascending entries; -1 if none).
+__device__ __forceinline__ int seq_of_row(const int32_t* qsl, int num_seqs, int tok) {
+  int lo = 0, hi = num_seqs;   // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(qsl + mid) <= tok) lo = mid;
+    else hi = mid;
+  }
+  return (num_seqs > 0 && __ldg(qsl + lo) <= tok && tok < __ldg(qsl + lo + 1)) ? lo : -1;
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

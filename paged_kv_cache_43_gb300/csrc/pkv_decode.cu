@@ -554,22 +554,53 @@ __global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs 
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= a.num_seqs * a.num_q_heads) return;
-  const int s = gw / a.num_q_heads;
-  const int hq = gw - s * a.num_q_heads;
-  const int L = __ldg(a.context_lens + s);
-  const int q0 = __ldg(a.query_start_loc + s);
-  const int qn = __ldg(a.query_start_loc + s + 1) - q0;
-  if (qn != 1 || q0 < 0 || q0 >= a.num_tokens || L < 1 ||
-      static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len ||
-      L <= a.key_begin_blocks * kBlock || (a.key_begin_blocks > 0 && q0 != s))
-    return;
-  const int kfirst = max((a.window > 0 && L > a.window) ? L - a.window : 0,
-                         a.key_begin_blocks * kBlock);
-  const int nblk_seq = (L + kBlock - 1) / kBlock - kfirst / kBlock;
-  // prefix partials (cascade) first, then this row's own splits
-  const int nsplit = a.prefix_splits + (nblk_seq + a.split_blocks - 1) / a.split_blocks;
-  if (nsplit <= 1 && !a.force_partial) return;  // the decode kernel wrote this row directly
-  const int64_t row = (static_cast<int64_t>(s) * a.num_q_heads + hq) * a.max_splits;
+  int q0, nsplit;
+  int64_t row;   // (query row, q head) index of the split partials
+  int hq;
+  if (a.merge_rows_end > a.merge_rows_begin) {
+    // Cascade merge of a chunked-prefill row: its prefix partials, then the
+    // one partial over its own keys.  A row whose sequence's metadata is bad
+    // (or that sits inside the shared prefix) is zeroed, as the attention
+    // calls do.
+    const int tok = a.merge_rows_begin + gw / a.num_q_heads;
+    hq = gw - (tok - a.merge_rows_begin) * a.num_q_heads;
+    q0 = tok;
+    const int s = seq_of_row(a.query_start_loc, a.casc_seqs, tok);
+    bool ok = s >= 0;
+    if (ok) {
+      const int L = __ldg(a.context_lens + s);
+      const int qn = __ldg(a.query_start_loc + s + 1) - __ldg(a.query_start_loc + s);
+      ok = qn >= 1 && L >= qn && static_cast<int64_t>(L) <= a.bt_stride * kBlock &&
+           L <= a.max_context_len && L - qn >= a.key_begin_blocks * kBlock;
+    }
+    if (!ok) {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
+                         (static_cast<int64_t>(tok) * a.num_q_heads + hq) * D + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; e += 2)
+        *reinterpret_cast<__nv_bfloat162*>(o + e) = __floats2bfloat162_rn(0.f, 0.f);
+      return;
+    }
+    nsplit = a.prefix_splits + 1;
+    row = (static_cast<int64_t>(tok) * a.num_q_heads + hq) * a.max_splits;
+  } else {
+    const int s = gw / a.num_q_heads;
+    hq = gw - s * a.num_q_heads;
+    const int L = __ldg(a.context_lens + s);
+    q0 = __ldg(a.query_start_loc + s);
+    const int qn = __ldg(a.query_start_loc + s + 1) - q0;
+    if (qn != 1 || q0 < 0 || q0 >= a.num_tokens || L < 1 ||
+        static_cast<int64_t>(L) > a.bt_stride * kBlock || L > a.max_context_len ||
+        L <= a.key_begin_blocks * kBlock || (a.key_begin_blocks > 0 && q0 != s))
+      return;
+    const int kfirst = max((a.window > 0 && L > a.window) ? L - a.window : 0,
+                           a.key_begin_blocks * kBlock);
+    const int nblk_seq = (L + kBlock - 1) / kBlock - kfirst / kBlock;
+    // prefix partials (cascade) first, then this row's own splits
+    nsplit = a.prefix_splits + (nblk_seq + a.split_blocks - 1) / a.split_blocks;
+    if (nsplit <= 1 && !a.force_partial) return;  // the decode kernel wrote this row directly
+    row = (static_cast<int64_t>(s) * a.num_q_heads + hq) * a.max_splits;
+  }
   const float* lse = a.ws_lse + row;
   float M = -INFINITY;
   for (int i = lane; i < nsplit; i += 32) M = fmaxf(M, lse[i]);

@@ -60,6 +60,12 @@ struct DecodeArgs {
   int32_t prefix_splits;         // combine: leading split slots that hold prefix partials
   int32_t prefix_len;            // prefix launch: the shared keys [0, prefix_len)
   int32_t prefix_col_groups;     // prefix launch: 8-column groups per kv head
+  // Combine over token rows [merge_rows_begin, merge_rows_end) (> begin: the
+  // cascade merge of chunked-prefill rows, each with prefix_splits prefix
+  // partials and one suffix partial); 0, 0 otherwise.
+  int32_t merge_rows_begin;
+  int32_t merge_rows_end;
+  int32_t casc_seqs;             // sequences of the batch (rows mode: row -> sequence)
   // Test hook (pkv_debug_wait_test): main-loop wait limit (0 = the default)
   // and, when set, warp 0 of every CTA withholds its first block load so
   // that its wait runs out.
@@ -104,6 +110,15 @@ struct PrefillArgs {
   int32_t max_splits;
   float* ws_o;
   float* ws_lse;
+  // Cascade prefix launch: the batch's sequences (query_start_loc has
+  // casc_seqs + 1 entries), to find each row's sequence for its descales.
+  int32_t casc_seqs;
+  // Cascade suffix launch of the tcgen05 kernel (key_begin > 0): every row
+  // sees only keys >= key_begin (the shared prefix is the prefix launch's),
+  // and writes its normalised fp32 partial and log2-sum-exp to ws_o / ws_lse
+  // at split slot split_base of rows [token, q head, max_splits].
+  int32_t key_begin;
+  int32_t split_base;
   // Test hook (pkv_debug_wait_test), tcgen05 kernel: main-loop wait limit (0
   // = the default) and, when set, the K producer withholds the CTA's first K
   // tile so that the waits for it run out.

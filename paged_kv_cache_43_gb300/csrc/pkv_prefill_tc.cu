@@ -307,8 +307,8 @@ __device__ __forceinline__ int tc_unit_cost(const PrefillArgs& a, int u, int tok
   if (qn <= 0 || tok0 >= qn || L < qn) return 0;   // nothing (or an error) to do
   const int pos_max = L - qn + min(tok0 + toks, qn) - 1;
   const int pos_min = L - qn + tok0;
-  const int j0 = (a.window > 0 && pos_min - a.window + 1 > 0)
-                     ? (pos_min - a.window + 1) / kTcKeys : 0;
+  const int lo_min = max(a.window > 0 ? pos_min - a.window + 1 : 0, a.key_begin);
+  const int j0 = lo_min > 0 ? lo_min / kTcKeys : 0;
   return (pos_max + kTcKeys) / kTcKeys - j0 + 1;   // key tiles + the CTA's own overhead
 }
 
@@ -401,9 +401,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0 && mtile == 0 && kvh == 0) raise_error(a.err, PKV_ERR_CONTEXT_LEN);
     return;
   }
-  if (!casc && (bad_len || qn > L || qn > a.max_query_len)) {
+  // (a cascade suffix row must sit after the shared prefix; its merge then
+  // zeroes the rows of the sequence)
+  const bool before_prefix = a.key_begin > 0 && L - qn < a.key_begin;
+  if (!casc && (bad_len || qn > L || qn > a.max_query_len || before_prefix)) {
     if (threadIdx.x == 0 && mtile == 0 && kvh == 0)
-      raise_error(a.err, bad_len ? PKV_ERR_CONTEXT_LEN : PKV_ERR_QUERY_LEN);
+      raise_error(a.err, (bad_len || before_prefix) ? PKV_ERR_CONTEXT_LEN : PKV_ERR_QUERY_LEN);
+    if (a.key_begin > 0) return;   // (the merge writes the output rows)
     const int nt = min(toks, qn - tok0);
     for (int i = threadIdx.x; i < nt * G * D; i += blockDim.x) {
       const int r = i / D;
@@ -421,9 +425,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // CTA walks tiles j0 .. ntiles-1, ring positions 0 .. n_rel-1.  A cascade
   // prefix CTA walks its split's prefix_tiles tiles.
   const int pos_min = L - qn + tok0;
+  // first key some row here sees: the lowest row's window start, or the end
+  // of the shared prefix (cascade suffix launch)
+  const int lo_min = max(a.window > 0 ? pos_min - a.window + 1 : 0, a.key_begin);
   const int j0 = casc ? static_cast<int>(blockIdx.z) * a.prefix_tiles
-                      : ((a.window > 0 && pos_min - a.window + 1 > 0)
-                             ? (pos_min - a.window + 1) / kTcKeys : 0);
+                      : (lo_min > 0 ? lo_min / kTcKeys : 0);
   const int ntiles =
       casc ? min(j0 + a.prefix_tiles, (L + kTcKeys - 1) / kTcKeys) : (pos_max + kTcKeys) / kTcKeys;
   const int n_rel = ntiles - j0;
@@ -431,7 +437,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // First cache block holding a key some row can see; blocks before it in
   // tile j0 are not loaded (their entries may be null) and their V rows are
   // zeroed instead.
-  const int lo_min = a.window > 0 ? pos_min - a.window + 1 : 0;
   const int b_lo = casc ? j0 * (kTcKeys / kBlock) : (lo_min > 0 ? lo_min / kBlock : 0);
   const int nblk = (pos_max + kBlock) / kBlock;
   // V rows of the first tile before the first loaded block, and of the last
@@ -807,8 +812,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float out_scale = 1.f;
     if constexpr (FP8) {
       // descales of this (sequence, kv head) -- a cascade prefix row's own
-      // sequence (row tok = sequence tok); this thread's Q row to fp16
-      const int ds = casc ? (valid ? tok : tok_last) : s;
+      // sequence (rows are the batch's query tokens); this thread's Q row to
+      // fp16
+      const int ds =
+          casc ? max(seq_of_row(a.query_start_loc, a.casc_seqs, valid ? tok : tok_last), 0) : s;
       sl2 *= __ldg(a.k_descale + static_cast<int64_t>(ds) * a.num_kv_heads + kvh);
       out_scale = __ldg(a.v_descale + static_cast<int64_t>(ds) * a.num_kv_heads + kvh);
       bool qok = warp_wait(q_full, 0, abort, a.err, wlim);
@@ -845,7 +852,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     float m_used = -INFINITY, l = 0.f;
     bool done = t < ntq;
-    const int lo = a.window > 0 ? pos - a.window + 1 : 0;  // first key in this row's window
+    // first key this row sees (its window; after the shared prefix in a
+    // cascade suffix launch)
+    const int lo = max(a.window > 0 ? pos - a.window + 1 : 0, a.key_begin);
     // Thread 0 of the warpgroup issues its tile's MMAs.  Handing them to
     // a separate MMA warp costs a wake-up per product, and that warp, sharing
     // its SM sub-partition with two softmax warps that have instructions ready
@@ -991,13 +1000,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (void)mbar_wait(drain, 0);
     }
     __syncwarp();
-    if (done && casc && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim)) {
-      // cascade prefix: the row's normalised partial and log2-sum-exp (in the
-      // scaled log2 domain of m_used) for the merge
+    if (done && (casc || a.key_begin > 0) &&
+        warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim)) {
+      // cascade prefix (split blockIdx.z) or suffix (split split_base): the
+      // row's normalised partial and log2-sum-exp (in the scaled log2 domain
+      // of m_used) for the merge
       tc::fence_after_sync();
       const float inv = l > 0.f ? out_scale / l : 0.f;
-      const int64_t wrow = (static_cast<int64_t>(tok) * Hq + kvh * G + g) * a.max_splits +
-                           blockIdx.z;
+      const int64_t wrow = (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * a.max_splits +
+                           (casc ? static_cast<int>(blockIdx.z) : a.split_base);
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];

@@ -294,18 +294,20 @@ def use_cascade(meta: AttnMeta, common_prefix_blocks: int) -> bool:
 
 
 def attention_cascade(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
-                      common_prefix_blocks, *, max_context_len, kv_split_tokens=0,
-                      workspace=None, stream=None) -> None:
-    """pkv_attention_cascade: a decode batch whose sequences share their first
-    ``common_prefix_blocks`` blocks; same result as attention()."""
+                      common_prefix_blocks, *, max_context_len, max_query_len=1,
+                      num_decode_seqs=-1, kv_split_tokens=0, workspace=None,
+                      stream=None) -> None:
+    """pkv_attention_cascade: a batch (decode rows, then chunked-prefill
+    sequences) whose sequences share their first ``common_prefix_blocks``
+    blocks; same result as attention()."""
     lib = load()
     for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _require(t, n, dtype=k_cache.dtype)
     _require(block_tables, "block_tables", dtype=torch.int32, ndim=2)
     _require(context_lens, "context_lens", dtype=torch.int32, ndim=1)
     _require(query_start_loc, "query_start_loc", dtype=torch.int32, ndim=1)
-    meta = attn_meta(q, block_tables, context_lens, max_query_len=1,
-                     max_context_len=max_context_len, num_decode_seqs=-1,
+    meta = attn_meta(q, block_tables, context_lens, max_query_len=max_query_len,
+                     max_context_len=max_context_len, num_decode_seqs=num_decode_seqs,
                      kv_split_tokens=kv_split_tokens)
     desc = cache_desc(k_cache)
     if workspace is None:
@@ -322,7 +324,8 @@ def attention_cascade(out, q, k_cache, v_cache, block_tables, context_lens, quer
 
 def attention_cascade_fp8(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
                           scale, common_prefix_blocks, k_descale, v_descale, *, max_context_len,
-                          kv_split_tokens=0, workspace=None, stream=None) -> None:
+                          max_query_len=1, num_decode_seqs=-1, kv_split_tokens=0,
+                          workspace=None, stream=None) -> None:
     """pkv_attention_cascade_fp8: attention_cascade over e4m3 caches with the
     descales of attention_fp8."""
     lib = load()
@@ -339,8 +342,8 @@ def attention_cascade_fp8(out, q, k_cache, v_cache, block_tables, context_lens, 
         _require(t, n, dtype=torch.float32, ndim=2)
         if tuple(t.shape) != (context_lens.shape[0], k_cache.shape[2]):
             raise PkvError(f"{n} must be [num_seqs, num_kv_heads]")
-    meta = attn_meta(q, block_tables, context_lens, max_query_len=1,
-                     max_context_len=max_context_len, num_decode_seqs=-1,
+    meta = attn_meta(q, block_tables, context_lens, max_query_len=max_query_len,
+                     max_context_len=max_context_len, num_decode_seqs=num_decode_seqs,
                      kv_split_tokens=kv_split_tokens)
     desc = cache_desc(k_cache)
     if workspace is None:

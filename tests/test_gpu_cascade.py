@@ -1,10 +1,11 @@
-"""Cascade attention on the GPU against the oracle: a decode batch whose
-sequences share their first P blocks, the prefix attended once for all rows
-(tcgen05 kernel when the group size divides 128 — G = 1, 4, 8 here — else
-the mma.sync decode kernel over (sequence, head) columns — G = 3), each row's
-own keys after it, the partials merged.  The result must be the
-plain attention (oracle) within the bf16 tolerance, and equal pkv_attention's
-within it."""
+"""Cascade attention on the GPU against the oracle: a batch whose sequences
+share their first P blocks, the prefix attended once for all rows (tcgen05
+kernel when the group size divides 128 -- G = 1, 4, 8 here -- else, for decode
+rows, the mma.sync decode kernel over (sequence, head) columns -- G = 3), each
+row's own keys after it (decode rows on the split-K decode kernel, chunked
+prefill rows causally on the tcgen05 kernel), the partials merged.  The
+result must be the plain attention (oracle) within the bf16 tolerance, and
+equal pkv_attention's within it."""
 import ctypes
 
 import numpy as np
@@ -218,5 +219,105 @@ def test_cascade_fp8_shapes_without_the_tcgen05_prefix_are_refused():
                                       max_context_len=g.max_context_len,
                                       workspace=torch.empty(1 << 20, dtype=torch.uint8,
                                                             device="cuda"))
+    torch.cuda.synchronize()
+    assert pkv.get_error() == 0
+
+
+# ------------------------------------------------- chunked-prefill rows
+
+def _shared_mixed(nd, chunks, pblocks, hq, hkv, d, seed, extra_hi=600):
+    """nd decode sequences then one chunk of each length in `chunks`, every
+    sequence sharing its first pblocks blocks; every query row after them."""
+    rng = np.random.default_rng(seed)
+    P = pblocks * 16
+    q_lens = [1] * nd + list(chunks)
+    ctx = [P + int(q) + int(rng.integers(0, extra_hi)) for q in q_lens]
+    return W.make_workload(q_lens, ctx, num_q_heads=hq, num_kv_heads=hkv, head_size=d,
+                           seed=seed, shared_prefix_blocks=pblocks,
+                           shared_seqs=tuple(range(len(q_lens))))
+
+
+MIXED = [(0, (1, 5, 97), 1, 8, 8, 128), (3, (17, 128, 200), 5, 32, 8, 128),
+         (6, (64, 511), 64, 32, 8, 128), (2, (40, 300), 17, 16, 1, 128),
+         (4, (33, 129), 5, 32, 8, 64), (1, (256,), 8, 128, 1, 128)]
+
+
+@pytest.mark.parametrize("nd,chunks,pblocks,hq,hkv,d", MIXED)
+def test_cascade_with_chunked_prefill_rows(nd, chunks, pblocks, hq, hkv, d):
+    """Decode rows and prefill chunks in one cascade call: every row of every
+    chunk equals the plain attention, and the oracle's own cascade split
+    (prefix state merged with the causal suffix state) agrees with both."""
+    wl = _shared_mixed(nd, chunks, pblocks, hq, hkv, d, seed=nd * 31 + pblocks + d)
+    exp, st, kc, vc = oracle_step(wl)
+    assert not st.any()
+    A = W.as_oracle_array
+    P = oracle.Problem(A(wl.q), kc, vc, A(wl.block_tables), A(wl.context_lens),
+                       A(wl.query_start_loc), wl.scale)
+    assert np.abs(oracle.cascade(P, pblocks * 16) - exp).max() < 1e-9
+    g, out = _cascade(wl, pblocks, max_query_len=wl.max_query_len, num_decode_seqs=nd)
+    assert max_err(out, exp) <= TOL[torch.bfloat16]
+    assert pkv.get_error() == 0
+
+
+@pytest.mark.parametrize("nd,chunks,pblocks,hq,hkv,d", MIXED[:3] + MIXED[4:5])
+def test_cascade_fp8_with_chunked_prefill_rows(nd, chunks, pblocks, hq, hkv, d):
+    from tests.support import fp8_scale_tensors, gpu_fp8_caches, oracle_step_fp8
+    wl = _shared_mixed(nd, chunks, pblocks, hq, hkv, d, seed=nd * 17 + pblocks + d)
+    g = wl.to("cuda")
+    S = g.num_seqs
+    ks, vs, _, _ = fp8_scale_tensors(hkv, S, 5)
+    rng = np.random.default_rng(nd + pblocks)
+    kd = torch.from_numpy(rng.uniform(0.002, 0.03, (S, hkv)).astype(np.float32)).cuda()
+    vd = torch.from_numpy(rng.uniform(0.005, 0.04, (S, hkv)).astype(np.float32)).cuda()
+    kc8, vc8 = gpu_fp8_caches(g, ks, vs)
+    pkv.write_fp8(g.k_new, g.v_new, g.slot_mapping, kc8, vc8, ks, vs)
+    out = nan_like(g.q)
+    pkv.attention_cascade_fp8(out, g.q, kc8, vc8, g.block_tables, g.context_lens,
+                              g.query_start_loc, g.scale, pblocks, kd, vd,
+                              max_context_len=g.max_context_len, max_query_len=g.max_query_len,
+                              num_decode_seqs=nd)
+    torch.cuda.synchronize()
+    exp, st, _, _ = oracle_step_fp8(wl, ks, vs, kd, vd)
+    assert not st.any()
+    assert max_err(out, exp) <= TOL[torch.bfloat16]
+    assert pkv.get_error() == 0
+
+
+def test_cascade_chunk_inside_the_prefix_is_zeroed_and_flagged():
+    """A chunk whose first row sits inside the shared prefix breaks the
+    cascade's contract: its rows come out zero with PKV_ERR_CONTEXT_LEN; the
+    other sequences are unaffected."""
+    wl = _shared_mixed(2, (40, 50), 4, 8, 2, 128, seed=3)
+    bad = 3                                          # the chunk of 50 rows
+    L = int(wl.ctx_lens[bad])
+    wl.ctx_lens[bad] = 4 * 16 + 10                   # L - q_len < 64 shared keys
+    wl.context_lens[bad] = int(wl.ctx_lens[bad])
+    good = [0, 1, 2]
+    exp, st, _, _ = oracle_step(wl)
+    g, out = _cascade(wl, 4, max_query_len=wl.max_query_len, num_decode_seqs=2)
+    qsl = wl.query_start_loc.numpy()
+    rows_good = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in good])
+    rows_bad = np.arange(qsl[bad], qsl[bad + 1])
+    assert max_err(out, exp, rows_good) <= TOL[torch.bfloat16]
+    assert not out[torch.from_numpy(rows_bad).cuda()].float().any()
+    assert pkv.get_error(clear=True) & (1 << 2)
+    assert L > 0
+
+
+def test_cascade_chunk_rows_refused_without_their_kernels():
+    g = _shared_mixed(1, (20,), 4, 12, 4, 128, seed=4).to("cuda")     # group 3
+    with pytest.raises(pkv.PkvError):
+        pkv.attention_cascade(torch.zeros_like(g.q), g.q, g.k_cache, g.v_cache, g.block_tables,
+                              g.context_lens, g.query_start_loc, g.scale, 4,
+                              max_context_len=g.max_context_len, max_query_len=20,
+                              num_decode_seqs=1,
+                              workspace=torch.empty(1 << 24, dtype=torch.uint8, device="cuda"))
+    g = _shared_mixed(1, (20,), 4, 8, 2, 128, seed=5).to("cuda")
+    with pytest.raises(pkv.PkvError):                                  # decode count unknown
+        pkv.attention_cascade(torch.zeros_like(g.q), g.q, g.k_cache, g.v_cache, g.block_tables,
+                              g.context_lens, g.query_start_loc, g.scale, 4,
+                              max_context_len=g.max_context_len, max_query_len=20,
+                              num_decode_seqs=-1,
+                              workspace=torch.empty(1 << 24, dtype=torch.uint8, device="cuda"))
     torch.cuda.synchronize()
     assert pkv.get_error() == 0
