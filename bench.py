@@ -891,19 +891,57 @@ def run_cascade_bench(args, device):
                       num_decode_seqs=wl.num_decode_seqs - nsh, workspace=ws2)
     attn_b, _, _ = algorithmic_bytes(wl)
     shared_dup = (nsh - 1) * Pb * 16 * 8 * 128 * 2 * 2
+    wl4_shared = Pb
     for name, fn in (("plain", plain4), ("cascade", casc4)):
         ms = _time_calls(fn, args.steps, args.warmup, stream)
         res[f"mixed4_{name}"] = {"attention_ms": round(ms, 5),
                                  "logical_GBs": round(attn_b / ms / 1e6, 1),
                                  "unique_GBs": round((attn_b - shared_dup) / ms / 1e6, 1)}
+    del wl, out, ws, ws2
+    # (3) a mixed batch where every sequence shares the prefix (48 decode rows
+    # and 4 chunks of 512 tokens after it): one cascade call against one plain
+    # call, prefixes of 1024 and 4096 tokens
+    for Pb in (64, 256):
+        rng = np.random.default_rng(99 + Pb)
+        q_lens = np.array([1] * 48 + [512] * 4, np.int64)
+        ctx = Pb * 16 + q_lens + rng.integers(0, 2048, 52, endpoint=True)
+        wl = W.make_workload(q_lens, ctx, num_q_heads=32, num_kv_heads=8, head_size=128,
+                             seed=99 + Pb, device=device, shared_prefix_blocks=Pb,
+                             shared_seqs=tuple(range(52)))
+        pkv.write(wl.k_new, wl.v_new, wl.slot_mapping, wl.k_cache, wl.v_cache)
+        out = torch.empty_like(wl.q)
+        kw = dict(max_query_len=wl.max_query_len, max_context_len=wl.max_context_len,
+                  num_decode_seqs=48)
+        meta = pkv.attn_meta(wl.q, wl.block_tables, wl.context_lens, **kw)
+        ws = torch.empty(max(pkv.workspace_size(wl.k_cache, meta),
+                             pkv.cascade_workspace_size(wl.k_cache, meta, Pb)),
+                         dtype=torch.uint8, device=device)
+        plain = lambda: pkv.attention(out, wl.q, wl.k_cache, wl.v_cache, wl.block_tables,  # noqa: E731
+                                      wl.context_lens, wl.query_start_loc, wl.scale,
+                                      workspace=ws, **kw)
+        casc = lambda: pkv.attention_cascade(out, wl.q, wl.k_cache, wl.v_cache,  # noqa: E731
+                                             wl.block_tables, wl.context_lens,
+                                             wl.query_start_loc, wl.scale, Pb, workspace=ws,
+                                             **kw)
+        flops = sum(int((c - q + np.arange(q) + 1).sum()) for q, c in zip(q_lens, ctx)) * 32 * 512
+        for name, fn in (("plain", plain), ("cascade", casc)):
+            ms = _time_calls(fn, args.steps, args.warmup, stream)
+            res[f"mixed_shared{Pb * 16}_{name}"] = {
+                "attention_ms": round(ms, 5), "TFLOPs": round(flops / ms / 1e9, 1),
+                "cascade_gate": int(pkv.use_cascade(meta, Pb))}
+        del wl, out, ws
     if pkv.get_error(clear=True):
         raise RuntimeError("device error word set")
     return {"metric": "cascade attention vs pkv_attention on shared-prefix batches",
             "unit": "ms / GB/s", "results": res,
             "config": {"shared2048": "64 decode seqs, 2048 shared + U[128,2048] own keys, "
                                      "32q/8kv, D=128 bf16 (and e4m3: GB/s over 1-byte codes)",
-                       "mixed4": f"workload 4: cascade for its {nsh} sequences sharing {Pb} "
-                                 "blocks, pkv_attention for the rest"},
+                       "mixed4": f"workload 4: cascade for its {nsh} sequences sharing "
+                                 f"{wl4_shared} blocks, pkv_attention for the rest",
+                       "mixed_sharedP": "48 decode rows + 4 chunks of 512, every sequence "
+                                        "sharing P tokens, own keys U[0, 2048] + the chunk; "
+                                        "one cascade call vs one plain call (TFLOP/s over "
+                                        "4 D flops per row and visible key)"},
             "steps": args.steps, "warmup": args.warmup}
 
 

@@ -283,11 +283,12 @@ int pkv_attention_cascade_fp8(void *out, const void *q, const void *k_cache,
                               const pkv_attn_meta *meta, void *workspace, size_t workspace_bytes,
                               void *stream);
 /* Whether to use cascade attention, host only.  1 when the [book]'s gate
- * passes (common prefix >= 256 tokens, >= 8 sequences, no sliding window; and,
- * for this build, decode rows only and a prefix shorter than the longest
- * context) and a cost rule measured on GB300 says it pays: prefix >= 512
- * tokens and (num_seqs - 1) * prefix tokens >= 16384 (the [book]'s own rule
- * is a rough CTA/wave model); else 0. */
+ * passes (common prefix >= 256 tokens, >= 8 sequences, no sliding window, a
+ * prefix shorter than the longest context) and a cost rule measured on GB300
+ * says it pays (the [book]'s own rule is a rough CTA/wave model): decode
+ * batches, prefix >= 512 tokens and (num_seqs - 1) * prefix tokens >= 16384;
+ * batches with chunked-prefill rows (num_decode_seqs given), at most 512
+ * chunk rows and a prefix >= 4096 tokens; else 0. */
 int pkv_use_cascade(const pkv_attn_meta *meta, int32_t common_prefix_blocks);
 
 /* Reads (and, if clear != 0, resets) the current device's error word: the OR

@@ -669,21 +669,31 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
 
 extern "C" int pkv_use_cascade(const pkv_attn_meta* meta, int32_t common_prefix_blocks) {
   // The gate the [book] gives for cascade attention: a common prefix of at
-  // least 256 tokens, at least 8 requests, no sliding window; this build's
-  // cascade also takes decode rows only.  Then, in place of the pages' rough
-  // CTA/wave model, one measured on GB300 (32 q / 8 kv heads, head_size 128,
-  // own keys U[128, 1024]; the prefix launch on the side stream beside the
-  // suffix launch): the plain call already meets repeated prefix reads in L2,
-  // so the cascade wins once the prefix is >= 512 tokens and the repeated
-  // prefix keys (sequences - 1) x prefix reach 16K (1.09x at 64 x 512, 1.17x
-  // at 16 x 2048, 1.19x at 8 x 8192, 3.6x at 64 x 8192, 6.0x at 256 x 8192;
-  // 0.83-0.96x below, and at every 256-token prefix).
+  // least 256 tokens, at least 8 requests, no sliding window.  Then, in place
+  // of the pages' rough CTA/wave model, rules measured on GB300 (32 q / 8 kv
+  // heads, head_size 128; the prefix launch on the side stream beside the
+  // suffix launches):
+  //  * decode rows (own keys U[128, 1024]): the plain call already meets
+  //    repeated prefix reads in L2, so the cascade wins once the prefix is
+  //    >= 512 tokens and the repeated prefix keys (sequences - 1) x prefix
+  //    reach 16K (1.09x at 64 x 512, 1.17x at 16 x 2048, 1.19x at 8 x 8192,
+  //    3.6x at 64 x 8192, 6.0x at 256 x 8192; 0.83-0.96x below, and at every
+  //    256-token prefix);
+  //  * with chunked-prefill rows: their prefix work is a dense contraction
+  //    either way (the cascade saves K/V reads, not flops) and costs a second
+  //    pass and a merge, so the cascade wins only for at most 512 chunk rows
+  //    beside a prefix of >= 4096 tokens (1.14-1.22x with 0, 16 or 48 decode
+  //    rows; 4 x 512 chunk rows: 0.58-0.93x at every prefix up to 4096).
   if (meta == nullptr) return 0;
   const int64_t p = static_cast<int64_t>(common_prefix_blocks) * kBlock;
   const bool pages_gate = p >= 256 && meta->num_seqs >= 8 && meta->sliding_window == 0;
-  const bool this_build = meta->max_query_len <= 1 && p < meta->max_context_len;
-  const bool pays = p >= 512 && (static_cast<int64_t>(meta->num_seqs) - 1) * p >= 16384;
-  return pages_gate && this_build && pays ? 1 : 0;
+  const bool chunks = meta->max_query_len > 1;
+  if (!pages_gate || p >= meta->max_context_len) return 0;
+  if (!chunks)
+    return p >= 512 && (static_cast<int64_t>(meta->num_seqs) - 1) * p >= 16384 ? 1 : 0;
+  if (meta->num_decode_seqs < 0 || meta->num_decode_seqs > meta->num_seqs) return 0;
+  const int64_t chunk_rows = static_cast<int64_t>(meta->num_tokens) - meta->num_decode_seqs;
+  return chunk_rows <= 512 && p >= 4096 ? 1 : 0;
 }
 
 extern "C" size_t pkv_attention_cascade_workspace_size(const pkv_cache_desc* cache,

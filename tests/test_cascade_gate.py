@@ -1,6 +1,7 @@
 """The cascade gate (pkv_use_cascade) on the host: the pages' conditions
 (>= 256 shared tokens, >= 8 sequences, no sliding window) plus this build's
-(decode rows, a key after the prefix) and the cost rule measured on GB300."""
+(a key after the prefix) and the cost rules measured on GB300 (decode rows;
+chunked-prefill rows)."""
 import pytest
 
 from paged_kv_cache_43_gb300 import build, pkv
@@ -36,6 +37,30 @@ def test_gate(S, mcl, pblocks, want):
     assert pkv.use_cascade(M(S, mcl), pblocks) == want
 
 
-def test_gate_rejects_window_and_prefill_rows():
+def test_gate_rejects_windows():
     assert not pkv.use_cascade(M(64, 3000, w=64), 128)
-    assert not pkv.use_cascade(M(64, 3000, mq=2), 128)
+
+
+def Mx(nd, chunk_rows, mcl, mq):
+    # nd decode sequences then chunked-prefill sequences holding chunk_rows rows
+    S = nd + max(1, chunk_rows // mq)
+    return pkv.AttnMeta(S, nd + chunk_rows, 8, 600, mq, mcl, nd, 0, 0)
+
+
+@pytest.mark.parametrize("nd,rows,mq,mcl,pblocks,want", [
+    (48, 512, 512, 7000, 256, True),    # one 512-token chunk, 4096 shared (measured 1.14x)
+    (16, 512, 512, 7000, 256, True),    # (1.14x)
+    (47, 512, 512, 7000, 256, True),    # >= 8 sequences either way
+    (48, 512, 512, 5000, 128, False),   # 2048 shared: 0.90x
+    (48, 2048, 512, 7000, 256, False),  # 4 x 512 chunk rows: 0.93x
+    (16, 2048, 256, 7000, 256, False),  # 8 x 256: 0.81x
+    (48, 512, 512, 7000, -1, False),    # (no prefix)
+])
+def test_gate_with_chunk_rows(nd, rows, mq, mcl, pblocks, want):
+    assert pkv.use_cascade(Mx(nd, rows, mcl, mq), max(pblocks, 0)) == want
+
+
+def test_gate_with_chunk_rows_needs_the_decode_count():
+    m = Mx(48, 512, 7000, 512)
+    m.num_decode_seqs = -1
+    assert not pkv.use_cascade(m, 256)
