@@ -671,7 +671,9 @@ PER_WORKLOAD = [(3, False), (4, False), (5, False), (2, True), (3, True), (4, Tr
 
 def profile_only(args, kv):
     """Warm-up then `steps` plain steps, nothing else: a short, fixed launch
-    sequence for ncu captures (not a bench measurement)."""
+    sequence for ncu captures (not a bench measurement).  --part prefill or
+    decode: after one whole step, only that part's attention call (the prefill
+    sequences alone launch their CTAs longest first)."""
     from paged_kv_cache_43_gb300 import pkv
     wl = kv.wl
     out = torch.empty_like(wl.q)
@@ -679,12 +681,22 @@ def profile_only(args, kv):
     ws = torch.empty(max(pkv.workspace_size(kv.k, meta), 1), dtype=torch.uint8,
                      device=wl.q.device)
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup + args.steps):
+    if args.part == "all":
+        for _ in range(args.warmup + args.steps):
+            kv.step(out, ws, stream)
+    else:
         kv.step(out, ws, stream)
+        nd = wl.num_decode_seqs
+        s0, s1 = (nd, wl.num_seqs) if args.part == "prefill" else (0, nd)
+        if s0 == s1:
+            raise SystemExit(f"workload {wl.name} has no {args.part} sequences")
+        call, _ = kv.part_timer(s0, s1, stream)
+        for _ in range(args.warmup + args.steps):
+            call()
     torch.cuda.synchronize()
     if pkv.get_error(clear=True):
         raise RuntimeError("device error word set")
-    print(json.dumps({"profile_run": wl.name, "kv_cache_dtype": args.kv_dtype,
+    print(json.dumps({"profile_run": wl.name, "kv_cache_dtype": args.kv_dtype, "part": args.part,
                       "num_seqs": wl.num_seqs, "steps": args.warmup + args.steps}), flush=True)
     return None
 
@@ -1108,6 +1120,8 @@ def main():
                     help="time the host block pool (C++ vs oracle) on a serving trace; no GPU")
     ap.add_argument("--profile", action="store_true",
                     help="run warmup+steps plain steps only (for ncu), print no bench line")
+    ap.add_argument("--part", choices=["all", "prefill", "decode"], default="all",
+                    help="--profile: the whole step, or one part's attention call alone")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

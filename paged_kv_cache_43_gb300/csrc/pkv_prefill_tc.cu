@@ -14,24 +14,32 @@
 //    holds 128/G tokens x G heads and is one TMA load per 64-column half
 //    (box 64 x G heads x 128/G tokens, 128-byte swizzle), which lands exactly
 //    in the K-major UMMA layout.
-//  * warp 0 streams 128-key K and V tiles (8 cache blocks, one TMA box per
-//    block and half) into a 3-deep K ring and a 2-deep V ring (K is needed by
-//    the first product, V only by the second) shared by both query tiles; warp 1
-//    allocates all 512 TMEM columns and one of its threads issues every MMA:
+//  * 12 warps.  Warp 8 streams 128-key K tiles and warp 10 V tiles (8 cache
+//    blocks, one TMA box per block and half; block ids fetched four tiles
+//    ahead) into a 3-deep K ring and a 2-deep V ring (K is needed by the
+//    first product, V only by the second) shared by both query tiles; warp 9
+//    allocates all 512 TMEM columns.  The products of query tile t,
 //        S_t  = Q_t K^T   (M=128, N=128, K=16 x D/16, operands from smem)
 //        O_t += P_t V     (M=128, N=D,   K=16 x 8, P_t from TMEM, V MN-major)
-//    An M=128 tcgen05 MMA takes the same time for any N <= 256, so the tiles
-//    are as wide as TMEM allows: S_t (128 columns) and O_t (D columns) per
-//    query tile fill the 512 columns, and P_t (bf16) is written over the
-//    first half of S_t's columns.  S_t of the next K/V tile is issued once
-//    P_t V has completed; meanwhile the tensor core runs the other query
-//    tile's products, so it is never waiting on one softmax.
-//  * warps 2-5 and 6-9 (one warpgroup per query tile) own one TMEM lane
+//    are issued by one thread of tile t's own softmax warpgroup right after
+//    it has written P_t, each group of eight K-steps from one asm block: an
+//    issuing thread whose SM sub-partition neighbours keep the FMA pipe busy
+//    gets few issue slots (measured), and the warpgroup that has just
+//    finished its softmax is the one whose instructions are ready.  The two
+//    tiles take turns (S_0, S_1, then [P_0 V, S_0], [P_1 V, S_1], ...), so one
+//    tile's softmax runs beside the other tile's products.  An M=128
+//    tcgen05 MMA at N = 128 runs at the full rate (64 cycles per K-step),
+//    S_t (128 columns) and O_t (D columns) per query tile fill the 512
+//    columns, and P_t (bf16) is written over the first half of S_t's columns;
+//    S_t of the next K/V tile follows P_t V in the same thread's order.
+//  * warps 0-3 and 4-7 (one warpgroup per query tile) own one TMEM lane
 //    (= one row) per thread: they load a row of S, apply the causal mask, keep
 //    a lazily updated running max (O is rescaled in TMEM only when the max
 //    grows by more than 2^8), write P (bf16) to TMEM for the second MMA, and at
 //    the end read O, divide by the row sum and store bf16.  No shuffles: a
-//    thread holds its whole row.
+//    thread holds its whole row.  The V producer zeroes the rows of the first
+//    and last V tiles that no row may see (stale data, NaN included, would
+//    reach P V through 0 * NaN).
 //  * a launch that has the GPU to itself hands its CTAs out longest first
 //    (each CTA ranks the (sequence, tile pair) units by the key tiles they
 //    see and takes the one whose rank is its launch index), so the last wave
@@ -59,35 +67,20 @@ constexpr int kTcRows = 128;      // UMMA M (rows of one query tile)
 constexpr int kTcTiles = 2;       // query tiles per CTA
 constexpr int kTcKeys = 128;      // keys per K/V tile
 // Warps: 0-3 softmax of query tile 0, 4-7 of query tile 1 (warpgroups 0 and
-// 1: warp w reads TMEM lanes 32 (w % 4) ..), 8 the TMA producer, 9 the MMA
-// issuer, 10-11 widen e4m3 K and V tiles (FP8 cache; idle otherwise).  The
-// launch gives each thread 168 registers; warpgroup 2 then hands registers
-// back so that the softmax warpgroups run at 208 (2 x 128 x 208 + 128 x 80 =
+// 1: warp w reads TMEM lanes 32 (w % 4) ..), 8 the K producer (and the V
+// producer with an FP8 cache), 9 TMEM allocation, 10 the V producer (bf16) or
+// the K widener (FP8), 11 the V widener (FP8; idle otherwise).  The launch
+// gives each thread 168 registers; warpgroup 2 then hands registers back so
+// that the softmax warpgroups run at 208 (2 x 128 x 208 + 128 x 80 =
 // 384 x 168).
 constexpr int kTcThreads = 384;
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsOther = 80;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kTcThreads * 168, "register split");
-// Of every 8 packed pairs of scores, this many are exponentiated by the
-// polynomial on the FMA pipe and the rest by the MUFU.
-#ifndef PKV_TC_EMU_PAIRS
-#define PKV_TC_EMU_PAIRS 0
-#endif
-constexpr int kEmuPairs = PKV_TC_EMU_PAIRS;
-// Each softmax warpgroup issues its own tile's MMAs (1), or warp 9 issues
-// both tiles' from an event loop (0).
-#ifndef PKV_TC_SELF_ISSUE
-#define PKV_TC_SELF_ISSUE 1
-#endif
-constexpr bool kSelfIssue = PKV_TC_SELF_ISSUE != 0;
-#ifndef PKV_TC_KSTAGES
-#define PKV_TC_KSTAGES 3
-#endif
-#ifndef PKV_TC_VSTAGES
-#define PKV_TC_VSTAGES 2
-#endif
-constexpr int kKStages = PKV_TC_KSTAGES;   // K ring depth
-constexpr int kVStages = PKV_TC_VSTAGES;   // V ring depth
+// Ring depths (measured on GB300: 3 K + 2 V stages equal 2 + 3 with a bf16
+// cache and beat them by 12-15 % with an e4m3 one).
+constexpr int kKStages = 3;   // K ring depth
+constexpr int kVStages = 2;   // V ring depth
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S of tile t at 128t (P of tile t over its first 64 columns),
 // O of tile t at 256 + 128t.
@@ -459,7 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(q_full, 1);
     // one MMA-issuing thread per query tile, each committing its own
     // products (or one thread issuing both tiles')
-    const uint32_t issuers = kSelfIssue ? static_cast<uint32_t>(ntq) : 1u;
+    const uint32_t issuers = static_cast<uint32_t>(ntq);
     mbar_init(drain, issuers);
     mbar_init(smem_u32(&sh->q_conv), 8);   // one arrival per softmax warp
     for (int t = 0; t < kTcTiles; ++t) {
@@ -694,83 +687,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (warp == 8 && lane == 0) (void)mbar_wait(q_full, 0);   // the query tiles too
     __syncwarp();
-   } else if (warp == 9 && !kSelfIssue) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      {
-        // Event loop: issue whichever MMA is ready, never blocking on one
-        // query tile while the other could use the tensor core.  No barrier
-        // phase can run more than one ahead of what this thread has seen, so
-        // parity probes are unambiguous.
-        int s_next[kTcTiles] = {0, 0};   // next tile index whose S is issued
-        int pv_next[kTcTiles] = {0, 0};  // next tile index whose P V is issued
-        int k_released = 0, v_released = 0;  // ring stages handed back to the producer
-        bool ok = wait_or_abort(q_ready, 0, abort, a.err, wlim);
-        uint64_t idle_since = 0;
-        while (ok) {
-          bool progress = false;
-  #pragma unroll
-          for (int t = 0; t < kTcTiles; ++t) {   // (unrolled: the counters stay in registers)
-            if (t >= ntq) break;
-            const int jp = pv_next[t];
-            if (jp < s_next[t] && mbar_test(smem_u32(&sh->p_full[t]), jp & 1) &&
-                mbar_test(smem_u32(&sh->v_full[jp % kVStages]), (jp / kVStages) & 1)) {
-              tc::fence_after_sync();
-              TC_MARK(500 + 64 * t + (jp & 63));
-              issue_pv(t, jp);
-              pv_next[t] = jp + 1;
-              progress = true;
-            }
-            const int js = s_next[t];
-            // S_t(js) overwrites the columns P_t(js - 1) lives in.  MMAs issued
-            // by one thread execute in issue order, so issuing it right after
-            // P_t(js - 1) V is enough; doing so at once makes the tensor-core
-            // order P0 V, S0, P1 V, S1 and offsets the two softmaxes by half a
-            // period, so one runs while the other tile's products do.
-            if (js < n_rel && pv_next[t] == js &&
-                mbar_test(smem_u32(&sh->k_full[js % kKStages]), (js / kKStages) & 1)) {
-              tc::fence_after_sync();
-              TC_MARK(300 + 64 * t + (js & 63));
-              issue_s(t, js);
-              s_next[t] = js + 1;
-              progress = true;
-            }
-          }
-          int done_s = s_next[0], done_pv = pv_next[0];
-          if (ntq > 1) {
-            done_s = min(done_s, s_next[1]);
-            done_pv = min(done_pv, pv_next[1]);
-          }
-          while (k_released < done_s) {  // both S products of that K tile issued
-            tc::commit(smem_u32(&sh->k_empty[k_released % kKStages]));
-            ++k_released;
-          }
-          while (v_released < done_pv) {  // both P V products of that V tile issued
-            tc::commit(smem_u32(&sh->v_empty[v_released % kVStages]));
-            ++v_released;
-          }
-          if (done_pv == n_rel) break;
-          if (progress) {
-            idle_since = 0;
-          } else {
-            const uint64_t now = global_timer_ns();
-            if (idle_since == 0) {
-              idle_since = now;
-            } else if (*abort) {
-              ok = false;
-            } else if (now - idle_since > wlim) {
-              *abort = 1;
-              raise_error(a.err, PKV_ERR_TIMEOUT);
-              ok = false;
-            }
-          }
-        }
-        // Every MMA issued here must finish before TMEM is released.
-        tc::commit(drain);
-        (void)mbar_wait(drain, 0);
-      }
-    }
-    __syncwarp();
    } else if (FP8 && warp >= 10) {
     // ------------------------------------------------- widen e4m3 tiles (FP8)
     const bool is_v = warp == 11;
@@ -870,9 +786,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // contend).  issued[t] completes one phase per group tile t has issued,
     // its S(0) being phase 0; a turn waits for the other tile's previous
     // group, which cannot run two phases ahead of the waiter.
-    constexpr bool self_issue = kSelfIssue;
     // (tile t's issuer sits on SM sub-partition t, apart from the other tile's)
-    const bool issuer = self_issue && done && quarter == t && lane == 0;
+    const bool issuer = done && quarter == t && lane == 0;
     const bool paired = ntq > 1;
     const uint32_t my_issued = smem_u32(&sh->issued[t]);
     const uint32_t other_issued = smem_u32(&sh->issued[t ^ 1]);
@@ -951,12 +866,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int k = 2 * (c0 + c);
           float y0, y1;
           tc::fma_f32x2(x[k], x[k + 1], m2, b2, y0, y1);
-          if ((c & 7) < kEmuPairs) {
-            tc::exp2_poly_x2(y0, y1);
-          } else {
-            y0 = ex2(y0);
-            y1 = ex2(y1);
-          }
+          y0 = ex2(y0);
+          y1 = ex2(y1);
           pk[c] = pack2<FP8>(y0, y1);
           tc::add_f32x2(acc[c & 3], y0, y1);
         }

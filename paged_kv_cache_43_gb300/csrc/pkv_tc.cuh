@@ -213,48 +213,6 @@ __device__ __forceinline__ void add_f32x2(uint64_t& acc, float x0, float x1) {
       : "f"(x0), "f"(x1));
 }
 
-// Lane-wise (y0, y1) = 2^(y0, y1) on the FMA pipe instead of the MUFU (which
-// does 16 results per clock per SM, as many as the tensor core needs per
-// 128x128 score tile): Cody-Waite range reduction y = j + f with j the
-// nearest integer (adding 1.5 * 2^23 rounds y into the low mantissa bits) and
-// |f| <= 1/2, a degree-3 polynomial for 2^f, and j added to the exponent
-// field.  The coefficients are this library's own minimax fit of 2^f on
-// [-1/2, 1/2] by a Remez exchange on the relative error: at most 7.5e-5,
-// 26x below the bf16/fp16 rounding every weight goes through before the P V
-// product.  Inputs are clamped to -126 so that masked (-inf) scores give 0 or
-// a subnormal below 2^-125; inputs never exceed 2^8 here.
-constexpr float kExp2C0 = 0.99992806f;
-constexpr float kExp2C1 = 0.69326097f;
-constexpr float kExp2C2 = 0.24261113f;
-constexpr float kExp2C3 = 0.05517167f;
-constexpr float kExp2Round = 12582912.0f;   // 1.5 * 2^23
-
-__device__ __forceinline__ void exp2_poly_x2(float& y0, float& y1) {
-  const float a0 = fmaxf(y0, -126.f), a1 = fmaxf(y1, -126.f);
-  uint32_t t0, t1;
-  float p0, p1;
-  asm("{\n\t.reg .b64 a, m, t, j, f, p, c;\n\t"
-      "mov.b64 a, {%4, %5};\n\t"
-      "mov.b64 m, {%6, %6};\n\t"
-      "add.rn.f32x2 t, a, m;\n\t"
-      "sub.rn.f32x2 j, t, m;\n\t"
-      "sub.rn.f32x2 f, a, j;\n\t"
-      "mov.b64 c, {%7, %7};\n\t"
-      "mov.b64 p, {%8, %8};\n\t"
-      "fma.rn.f32x2 p, c, f, p;\n\t"
-      "mov.b64 c, {%9, %9};\n\t"
-      "fma.rn.f32x2 p, p, f, c;\n\t"
-      "mov.b64 c, {%10, %10};\n\t"
-      "fma.rn.f32x2 p, p, f, c;\n\t"
-      "mov.b64 {%0, %1}, p;\n\t"
-      "mov.b64 {%2, %3}, t;\n\t}"
-      : "=f"(p0), "=f"(p1), "=r"(t0), "=r"(t1)
-      : "f"(a0), "f"(a1), "f"(kExp2Round), "f"(kExp2C3), "f"(kExp2C2), "f"(kExp2C1),
-        "f"(kExp2C0));
-  y0 = __uint_as_float(__float_as_uint(p0) + (t0 << 23));
-  y1 = __uint_as_float(__float_as_uint(p1) + (t1 << 23));
-}
-
 __device__ __forceinline__ float sum_f32x2(uint64_t v) {
   float lo, hi;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
