@@ -604,7 +604,7 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
     d.v_descale = v_descale;
     d.scale_log2 = scale * LOG2E;
     PKV_TRY(launch_decode_bf16(kmap, vmap, d, cache->head_size, fp8, st));
-    PKV_TRY(launch_combine_bf16(d, cache->head_size, st));
+    PKV_TRY(launch_combine_bf16(d, cache->head_size, st, /*after_decode=*/true));
     return PKV_OK;
   };
   auto prefill_part = [&](cudaStream_t st) -> int {

@@ -65,6 +65,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                            const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using T = DecodeTile<D, FP8>;
   constexpr int NW = kDecodeWarps;
+  // Every CTA of this grid is resident once it runs this: the combine launch
+  // that follows (programmatic, see launch_combine_bf16) may be scheduled
+  // beside the grid's last CTAs; it waits for the grid's completion itself.
+  asm volatile("griddepcontrol.launch_dependents;");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -551,6 +555,9 @@ template <int D>
 __global__ void __launch_bounds__(128) pkv_combine_bf16_kernel(const DecodeArgs a) {
   constexpr int PER = D / 32;  // elements per lane
   static_assert(PER == 2 || PER % 4 == 0, "head_size 64 or a multiple of 128");
+  // (a programmatic dependent launch: the decode grid's partials are visible
+  // once this returns; a no-op after an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= a.num_seqs * a.num_q_heads) return;
@@ -695,15 +702,28 @@ cudaError_t launch_cascade_prefix_bf16(const CUtensorMap& kmap, const CUtensorMa
   return launch_decode_t<64, 4, false, true>(kmap, vmap, a, stream);
 }
 
-cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream) {
+cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream,
+                                bool after_decode) {
   if (a.num_seqs == 0 || a.max_splits <= 1) return cudaSuccess;
   const int warps = a.num_seqs * a.num_q_heads;
   const int blocks = (warps + 3) / 4;
-  if (head_size == 128)
-    pkv_combine_bf16_kernel<128><<<blocks, 128, 0, stream>>>(a);
-  else
-    pkv_combine_bf16_kernel<64><<<blocks, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  // Right after the decode launch on the same stream, the combine is a
+  // programmatic dependent launch: its CTAs are scheduled while the decode's
+  // last CTAs still run and wait in griddepcontrol.wait for the decode
+  // grid's completion (its partials visible), so the launch gap overlaps the
+  // decode's tail instead of following it.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_decode ? 1 : 0;
+  if (head_size == 128) return cudaLaunchKernelEx(&cfg, pkv_combine_bf16_kernel<128>, a);
+  return cudaLaunchKernelEx(&cfg, pkv_combine_bf16_kernel<64>, a);
 }
 
 }  // namespace pkv

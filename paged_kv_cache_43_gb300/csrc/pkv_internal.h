@@ -157,7 +157,10 @@ cudaError_t launch_write_fp8(const WriteArgs& a, cudaStream_t stream, int num_sm
 cudaError_t launch_decode_bf16(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                const DecodeArgs& a, int head_size, bool fp8,
                                cudaStream_t stream);
-cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream);
+// after_decode: launched right after launch_decode_bf16 on the same stream
+// (a programmatic dependent launch; false when other work sits between them).
+cudaError_t launch_combine_bf16(const DecodeArgs& a, int head_size, cudaStream_t stream,
+                                bool after_decode = false);
 // Cascade prefix launch: every decode row of the batch (all sequences, all q
 // heads) against the shared prefix keys, read once per 8 columns; partials to
 // split slots [0, prefix_splits).
