@@ -99,7 +99,8 @@ struct TcLayout {
 };
 
 struct TcShared {
-  uint64_t q_full, drain, q_conv;
+  uint64_t q_full, q_conv;
+  uint64_t drain[kTcTiles];   // each tile's issuer: all its products complete
   uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t k_land[kKStages], v_land[kVStages];   // FP8: codes landed, not yet widened
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return lead > 0 || tail < kTcKeys;
   };
 
-  const uint32_t q_full = smem_u32(&sh->q_full), drain = smem_u32(&sh->drain);
+  const uint32_t q_full = smem_u32(&sh->q_full);
   // the MMAs may read Q once it has landed (bf16) or been converted (FP8)
   const uint32_t q_ready = FP8 ? smem_u32(&sh->q_conv) : q_full;
   if (threadIdx.x == 0) {
@@ -450,16 +451,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tensor_map(&kmap);
     prefetch_tensor_map(&vmap);
     mbar_init(q_full, 1);
-    // one MMA-issuing thread per query tile, each committing its own
-    // products (or one thread issuing both tiles')
+    // one MMA-issuing thread per query tile, each committing its own products
     const uint32_t issuers = static_cast<uint32_t>(ntq);
-    mbar_init(drain, issuers);
     mbar_init(smem_u32(&sh->q_conv), 8);   // one arrival per softmax warp
     for (int t = 0; t < kTcTiles; ++t) {
       mbar_init(smem_u32(&sh->s_full[t]), 1);
       mbar_init(smem_u32(&sh->p_full[t]), 4);
       mbar_init(smem_u32(&sh->pv_done[t]), 1);
       mbar_init(smem_u32(&sh->issued[t]), 1);
+      mbar_init(smem_u32(&sh->drain[t]), 1);
     }
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(smem_u32(&sh->k_full[i]), 1);
@@ -907,8 +907,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
     }
     if (issuer) {   // every MMA this thread issued completes before TMEM is freed
-      tc::commit(drain);
-      (void)mbar_wait(drain, 0);
+      tc::commit(smem_u32(&sh->drain[t]));
+      (void)mbar_wait(smem_u32(&sh->drain[t]), 0);
     }
     __syncwarp();
     if (done && (casc || a.key_begin > 0) &&
@@ -937,22 +937,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (valid) a.ws_lse[wrow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
     } else if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim)) {
       tc::fence_after_sync();
+      if (quarter == 0 && lane == 0) TC_MARK(1300 + t);
       const float inv = l > 0.f ? out_scale / l : 0.f;
       __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * D;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tc::ld32(tO + c0, o);
-        tc::wait_ld();
-        if (valid) {
-          uint32_t w[16];
+      uint32_t o[D];   // the whole O row: every load in flight before one wait
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            w[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+      for (int c0 = 0; c0 < D; c0 += 32)
+        tc::ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(o + c0));
+      tc::wait_ld();
+      if (valid) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        for (int c0 = 0; c0 < D; c0 += 8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            w[c] = pack_bf16(__uint_as_float(o[c0 + 2 * c]) * inv,
+                             __uint_as_float(o[c0 + 2 * c + 1]) * inv);
+          *reinterpret_cast<uint4*>(orow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }
