@@ -633,11 +633,14 @@ int attention_impl(void* out, const void* q, const void* k_cache, const void* v_
       // tcgen05/TMEM kernel: two tiles of 128/G tokens x G heads per CTA.
       const int toks = prefill_tc_tokens_per_cta(G);
       f.num_mtiles = (meta->max_query_len + toks - 1) / toks;
-      CUtensorMap qmap;
+      CUtensorMap qmap, omap;
       if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
                                    cache->head_size, G))
         return e;
-      PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, st));
+      if (int e = encode_query_map(&omap, out, meta->num_tokens, meta->num_q_heads,
+                                   cache->head_size, G))
+        return e;
+      PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, omap, f, cache->head_size, fp8, st));
     } else {
       // group sizes that do not divide 128 rows: mma.sync kernel, 64 rows per
       // CTA.
@@ -846,7 +849,7 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
     if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
                                  cache->head_size, d.group))
       return e;
-    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, pst));
+    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, qmap, f, cache->head_size, fp8, pst));  // (no output map: workspace rows)
   } else {
     DecodeArgs pa = d;
     pa.split_blocks = p.prefix_split_blocks;
@@ -895,7 +898,7 @@ int cascade_impl(void* out, const void* q, const void* k_cache, const void* v_ca
     if (int e = encode_query_map(&qmap, q, meta->num_tokens, meta->num_q_heads,
                                  cache->head_size, d.group))
       return e;
-    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, f, cache->head_size, fp8, st));
+    PKV_TRY(launch_prefill_tc(qmap, kmap, vmap, qmap, f, cache->head_size, fp8, st));  // (workspace rows)
   }
   if (int e = fork.join()) return e;
   PKV_TRY(launch_combine_bf16(sa, cache->head_size, st));

@@ -176,10 +176,13 @@ cudaError_t launch_attention_f32(const F32Args& a, cudaStream_t stream);
 bool prefill_tc_supported(int head_size, int group);
 int prefill_tc_tokens_per_tile(int group);
 int prefill_tc_tokens_per_cta(int group);
-// fp8 = true: e4m3 caches (head_size 128 only), widened to fp16 in shared memory.
+// fp8 = true: e4m3 caches, widened to fp16 in shared memory.
+// omap: the output tensor viewed like qmap (full query tiles of a plain
+// launch leave through it; cascade launches write the workspace instead).
 cudaError_t launch_prefill_tc(const CUtensorMap& qmap, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, const PrefillArgs& a, int head_size,
-                              bool fp8, cudaStream_t stream);
+                              const CUtensorMap& vmap, const CUtensorMap& omap,
+                              const PrefillArgs& a, int head_size, bool fp8,
+                              cudaStream_t stream);
 
 // Rows of the prefill kernel's query tile (grid.x covers ceil(q_len*G / this)).
 constexpr int kPrefillRows = 64;

@@ -344,7 +344,8 @@ template <int D, bool FP8, bool LPT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     pkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
-                          const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+                          const __grid_constant__ CUtensorMap vmap,
+                          const __grid_constant__ CUtensorMap omap, const PrefillArgs a) {
   using Lt = TcLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -450,6 +451,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tensor_map(&qmap);
     prefetch_tensor_map(&kmap);
     prefetch_tensor_map(&vmap);
+    prefetch_tensor_map(&omap);
     mbar_init(q_full, 1);
     // one MMA-issuing thread per query tile, each committing its own products
     const uint32_t issuers = static_cast<uint32_t>(ntq);
@@ -820,10 +822,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // causal mask on raw scores (also hides keys >= L); scale > 0, so the
       // row max of the raw scores gives the max of the scaled ones
       const int key0 = (j0 + j) * kTcKeys;
-      if (key0 + kTcKeys - 1 > pos || key0 < lo) {
+      // (warp-uniform branches: the votes below need every lane)
+      if (__any_sync(0xffffffffu, key0 + kTcKeys - 1 > pos || key0 < lo)) {
+        // visible columns [nlo, nvis) of this row (rows that see the whole
+        // tile keep every column); one compare per element where no row of
+        // the warp has a lower bound in this tile
+        const int nvis = pos - key0 + 1;
+        const int nlo = lo - key0;
+        if (__any_sync(0xffffffffu, nlo > 0)) {
 #pragma unroll
-        for (int c = 0; c < kTcKeys; ++c)
-          x[c] = (key0 + c > pos || key0 + c < lo) ? -INFINITY : x[c];
+          for (int c = 0; c < kTcKeys; ++c)
+            x[c] = (c < nvis && c >= nlo) ? x[c] : -INFINITY;
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTcKeys; ++c) x[c] = c < nvis ? x[c] : -INFINITY;
+        }
       }
       // row max: four independent chains of three-input maxima
       float m4[4] = {x[0], x[1], x[2], x[3]};
@@ -911,41 +924,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (void)mbar_wait(smem_u32(&sh->drain[t]), 0);
     }
     __syncwarp();
-    if (done && (casc || a.key_begin > 0) &&
-        warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim)) {
-      // cascade prefix (split blockIdx.z) or suffix (split split_base): the
-      // row's normalised partial and log2-sum-exp (in the scaled log2 domain
-      // of m_used) for the merge
-      tc::fence_after_sync();
-      const float inv = l > 0.f ? out_scale / l : 0.f;
-      const int64_t wrow = (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * a.max_splits +
-                           (casc ? static_cast<int>(blockIdx.z) : a.split_base);
+    if (casc || a.key_begin > 0) {
+      if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim)) {
+        // cascade prefix (split blockIdx.z) or suffix (split split_base): the
+        // row's normalised partial and log2-sum-exp (in the scaled log2 domain
+        // of m_used) for the merge
+        tc::fence_after_sync();
+        const float inv = l > 0.f ? out_scale / l : 0.f;
+        const int64_t wrow = (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * a.max_splits +
+                             (casc ? static_cast<int>(blockIdx.z) : a.split_base);
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tc::ld32(tO + c0, o);
-        tc::wait_ld();
-        if (valid) {
-          float4* dst = reinterpret_cast<float4*>(a.ws_o + wrow * D + c0);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tc::ld32(tO + c0, o);
+          tc::wait_ld();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(a.ws_o + wrow * D + c0);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                 __uint_as_float(o[4 * v + 2]) * inv,
-                                 __uint_as_float(o[4 * v + 3]) * inv);
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                   __uint_as_float(o[4 * v + 2]) * inv,
+                                   __uint_as_float(o[4 * v + 3]) * inv);
+          }
         }
+        if (valid) a.ws_lse[wrow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
       }
-      if (valid) a.ws_lse[wrow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
-    } else if (done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim)) {
-      tc::fence_after_sync();
-      if (quarter == 0 && lane == 0) TC_MARK(1300 + t);
-      const float inv = l > 0.f ? out_scale / l : 0.f;
-      __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * D;
+    } else if (t < ntq) {
+      const bool ok = done && warp_wait(b_pvdone, (n_rel - 1) & 1, abort, a.err, wlim);
+      // every row of the tile is a query row of this sequence
+      const bool full_tile = tok0 + (t + 1) * tile_toks - 1 <= tok_last;
+      float inv = 0.f;
       uint32_t o[D];   // the whole O row: every load in flight before one wait
+      if (ok) {
+        tc::fence_after_sync();
+        if (quarter == 0 && lane == 0) TC_MARK(1300 + t);
+        inv = l > 0.f ? out_scale / l : 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32)
-        tc::ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(o + c0));
-      tc::wait_ld();
-      if (valid) {
+        for (int c0 = 0; c0 < D; c0 += 32)
+          tc::ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(o + c0));
+        tc::wait_ld();
+      }
+      if (full_tile) {
+        // The rows go out through the tile's Q slot (its products have all
+        // completed: pv_done's last phase covers every MMA of the tile), in
+        // the swizzled layout Q arrived in, then one TMA store per 64-column
+        // half -- a row per thread written straight to memory would make
+        // every store instruction touch 32 rows.
+        uint8_t* srow = sQ + t * Lt::kQTile + row * 128;
+        if (ok) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              w[c] = pack_bf16(__uint_as_float(o[c0 + 2 * c]) * inv,
+                               __uint_as_float(o[c0 + 2 * c + 1]) * inv);
+            const int h = c0 / 64, j = (c0 % 64) / 8;
+            *reinterpret_cast<uint4*>(srow + h * Lt::kQHalf + ((j ^ (row & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async();   // generic writes, then the TMA engine reads
+        }
+        // the tile's four warps (named barrier 1 + t); no store unless all wrote
+        const bool all = named_barrier_and(1 + t, 128, ok);
+        if (all && quarter == 0 && lane == 0) {
+#pragma unroll
+          for (int h = 0; h < Lt::kHalves; ++h)
+            tma_store_3d(&omap, smem_u32(sQ + t * Lt::kQTile + h * Lt::kQHalf), h * 64, kvh * G,
+                         q0 + tok0 + t * tile_toks);
+          bulk_commit_group();
+          bulk_wait_group_read0();   // shared memory stays until the reads are done
+        }
+      } else if (ok && valid) {
+        __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + tok) * Hq + kvh * G + g) * D;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 8) {
           uint32_t w[4];
@@ -985,7 +1036,7 @@ namespace {
 
 template <int D, bool FP8>
 cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                        const PrefillArgs& a, cudaStream_t stream) {
+                        const CUtensorMap& omap, const PrefillArgs& a, cudaStream_t stream) {
   constexpr int smem = tc_smem_bytes<D>();
   const bool lpt = a.longest_first && !a.cascade_prefix &&
                    static_cast<int64_t>(a.num_seqs) * a.num_mtiles <= kLptUnits;
@@ -999,7 +1050,7 @@ cudaError_t launch_tc_t(const CUtensorMap& qmap, const CUtensorMap& kmap, const 
   dim3 grid(a.num_mtiles, a.num_kv_heads, gz);
   PrefillArgs b = a;
   debug_wait_settings(&b.wait_limit_ns, &b.debug_stall);
-  kfn<<<grid, kTcThreads, smem, stream>>>(qmap, kmap, vmap, b);
+  kfn<<<grid, kTcThreads, smem, stream>>>(qmap, kmap, vmap, omap, b);
   return cudaGetLastError();
 }
 
@@ -1014,14 +1065,14 @@ int prefill_tc_tokens_per_tile(int group) { return kTcRows / group; }
 int prefill_tc_tokens_per_cta(int group) { return kTcTiles * kTcRows / group; }
 
 cudaError_t launch_prefill_tc(const CUtensorMap& qmap, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, const PrefillArgs& a, int head_size,
-                              bool fp8, cudaStream_t stream) {
+                              const CUtensorMap& vmap, const CUtensorMap& omap,
+                              const PrefillArgs& a, int head_size, bool fp8, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_mtiles == 0) return cudaSuccess;
   if (fp8)
-    return head_size == 128 ? launch_tc_t<128, true>(qmap, kmap, vmap, a, stream)
-                            : launch_tc_t<64, true>(qmap, kmap, vmap, a, stream);
-  if (head_size == 128) return launch_tc_t<128, false>(qmap, kmap, vmap, a, stream);
-  return launch_tc_t<64, false>(qmap, kmap, vmap, a, stream);
+    return head_size == 128 ? launch_tc_t<128, true>(qmap, kmap, vmap, omap, a, stream)
+                            : launch_tc_t<64, true>(qmap, kmap, vmap, omap, a, stream);
+  if (head_size == 128) return launch_tc_t<128, false>(qmap, kmap, vmap, omap, a, stream);
+  return launch_tc_t<64, false>(qmap, kmap, vmap, omap, a, stream);
 }
 
 }  // namespace pkv
