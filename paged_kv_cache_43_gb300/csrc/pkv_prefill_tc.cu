@@ -16,9 +16,9 @@
 //    in the K-major UMMA layout.
 //  * 12 warps.  Warp 8 streams 128-key K tiles and warp 10 V tiles (8 cache
 //    blocks, one TMA box per block and half; block ids fetched four tiles
-//    ahead) into a 3-deep K ring and a 2-deep V ring (K is needed by the
-//    first product, V only by the second) shared by both query tiles; warp 9
-//    allocates all 512 TMEM columns.  The products of query tile t,
+//    ahead) into one 5-slot ring shared by both query tiles, in the order the
+//    products read them (K_0, V_0, K_1, V_1, ...); warp 9 allocates all 512
+//    TMEM columns.  The products of query tile t,
 //        S_t  = Q_t K^T   (M=128, N=128, K=16 x D/16, operands from smem)
 //        O_t += P_t V     (M=128, N=D,   K=16 x 8, P_t from TMEM, V MN-major)
 //    are issued by one thread of tile t's own softmax warpgroup right after
@@ -40,6 +40,8 @@
 //    thread holds its whole row.  The V producer zeroes the rows of the first
 //    and last V tiles that no row may see (stale data, NaN included, would
 //    reach P V through 0 * NaN).
+//  * the outputs of a full query tile go out through its Q slot in shared
+//    memory and one TMA store per 64-column half.
 //  * a launch that has the GPU to itself hands its CTAs out longest first
 //    (each CTA ranks the (sequence, tile pair) units by the key tiles they
 //    see and takes the one whose rank is its launch index), so the last wave
@@ -48,8 +50,8 @@
 //    TMEM is freed on every path.
 //  * FP8 (e4m3) cache: TMA lands each tile's codes (128 keys x D bytes, the
 //    128- or 64-byte swizzle of the row width) in the first part of its ring
-//    slot and warp 10 (K) or 11 (V) widens them in place to fp16 in the bf16
-//    tiles' layout (e4m3 is exact in fp16; codes are read before the fp16
+//    slot and warps 10 and 11 (D = 128: half the rows each; D = 64: warp 10)
+//    widen them in place to fp16 in the bf16 tiles' layout (e4m3 is exact in fp16; codes are read before the fp16
 //    rows written over them), then marks the slot full for the MMAs;
 //    each softmax thread converts its own Q row to fp16 (a row beyond 2^14
 //    scaled by 2^-e, its scores by 2^e) and the MMAs run on fp16 operands with
@@ -69,7 +71,7 @@ constexpr int kTcKeys = 128;      // keys per K/V tile
 // Warps: 0-3 softmax of query tile 0, 4-7 of query tile 1 (warpgroups 0 and
 // 1: warp w reads TMEM lanes 32 (w % 4) ..), 8 the K producer (and the V
 // producer with an FP8 cache), 9 TMEM allocation, 10 the V producer (bf16) or
-// the K widener (FP8), 11 the V widener (FP8; idle otherwise).  The launch
+// a widener (FP8), 11 a widener (FP8, D = 128; idle otherwise).  The launch
 // gives each thread 168 registers; warpgroup 2 then hands registers back so
 // that the softmax warpgroups run at 208 (2 x 128 x 208 + 128 x 80 =
 // 384 x 168).
@@ -77,10 +79,16 @@ constexpr int kTcThreads = 384;
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsOther = 80;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kTcThreads * 168, "register split");
-// Ring depths (measured on GB300: 3 K + 2 V stages equal 2 + 3 with a bf16
-// cache and beat them by 12-15 % with an e4m3 one).
-constexpr int kKStages = 3;   // K ring depth
-constexpr int kVStages = 2;   // V ring depth
+// One ring of K/V tile slots, filled in the order the products read them:
+// K of key tile j is ring element 2j, V of key tile j element 2j + 1, element
+// e in slot e % kRing.  (Separate K and V rings of 3 + 2 slots left V on the
+// critical path: a V tile was issued only once the V two tiles back had been
+// read, and its copy, ~1.5-2 us from L2, still in flight when P was ready.)
+constexpr int kRing = 5;
+__host__ __device__ constexpr int ring_slot(int e) { return e % kRing; }
+__host__ __device__ constexpr uint32_t ring_phase(int e) {
+  return static_cast<uint32_t>((e / kRing) & 1);
+}
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S of tile t at 128t (P of tile t over its first 64 columns),
 // O of tile t at 256 + 128t.
@@ -102,18 +110,19 @@ struct TcShared {
   uint64_t q_full, q_conv;
   uint64_t drain[kTcTiles];   // each tile's issuer: all its products complete
   uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
-  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-  uint64_t k_land[kKStages], v_land[kVStages];   // FP8: codes landed, not yet widened
+  uint64_t kv_full[kRing], kv_empty[kRing];
+  uint64_t kv_land[kRing];   // FP8 (and bf16 V edge tiles): landed, not yet ready
   uint64_t issued[kTcTiles];   // tile t's issuer has issued its next MMA group
   uint32_t tmem_base;
   int32_t abort;
+  int32_t n_issued[2];   // bf16 producers: K / V tiles issued, for the drain
 };
 
 template <int D>
 constexpr int tc_smem_bytes() {
   // Whole-SM footprint: one CTA per SM (it owns all 512 TMEM columns).
   constexpr int need = 1024 + kTcTiles * TcLayout<D>::kQTile +
-                       (kKStages + kVStages) * TcLayout<D>::kTileBytes +
+                       kRing * TcLayout<D>::kTileBytes +
                        static_cast<int>(sizeof(TcShared));
   return need > 120 * 1024 ? need : 120 * 1024;
 }
@@ -186,13 +195,13 @@ __device__ __forceinline__ float ex2(float x) {
 // rows: a lane reads its 16-code chunk of 4 rows (4 loads in flight), and
 // only after the warp has read the whole batch does it write the batch's fp16
 // chunks (those of half 0 overwrite the same rows' codes); batches touch
-// disjoint rows.
-__device__ __forceinline__ void widen_tile_fp8(uint8_t* tile, int lane) {
+// disjoint rows, so two warps may widen batches [b0, b1) of the same tile.
+__device__ __forceinline__ void widen_tile_fp8(uint8_t* tile, int lane, int b0, int b1) {
   const int c = lane & 7;           // chunk: columns 16c .. 16c + 15
   const int j = 2 * (c & 3);        // its first 8-column chunk within the half
   uint8_t* half = tile + (c >> 2) * (kTcKeys * 128);
 #pragma unroll 1
-  for (int b = 0; b < kTcKeys / 16; ++b) {
+  for (int b = b0; b < b1; ++b) {
     uint4 codes[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -218,19 +227,22 @@ __device__ __forceinline__ void widen_tile_fp8(uint8_t* tile, int lane) {
   __syncwarp();
 }
 
-// Zeroes the V rows [0, lead) and [tail, 128) of one landed 128-key tile
-// (bf16 or widened fp16 layout: D / 64 halves of 128 rows x 128 B, 16 KB
-// apart); the calling warp's 32 lanes share the stores.  Those keys have
-// P = 0 in every row, but their rows may hold stale data -- NaN included --
-// which 0 * NaN would carry into P V.
+// Zeroes the V rows [0, lead) and [tail, 128) that lie in rows [r0, r1) of
+// one landed 128-key tile (bf16 or widened fp16 layout: D / 64 halves of 128
+// rows x 128 B, 16 KB apart); the calling warp's 32 lanes share the stores.
+// Those keys have P = 0 in every row, but their rows may hold stale data --
+// NaN included -- which 0 * NaN would carry into P V.
 template <int D>
-__device__ __forceinline__ void zero_v_rows(uint8_t* vt, int lead, int tail, int lane) {
+__device__ __forceinline__ void zero_v_rows(uint8_t* vt, int lead, int tail, int r0, int r1,
+                                            int lane) {
   constexpr int per_row = (D / 64) * 8;   // 16-byte chunks per row
-  const int nlead = lead > 0 ? lead : 0;
-  const int ntail = kTcKeys - tail;
+  const int lead_end = min(max(lead, r0), r1);   // lead rows: [r0, lead_end)
+  const int tail_beg = min(max(tail, r0), r1);   // tail rows: [tail_beg, r1)
+  const int nlead = lead_end - r0;
+  const int ntail = r1 - tail_beg;
   for (int e = lane; e < (nlead + ntail) * per_row; e += 32) {
     const int r = e / per_row;
-    const int key = r < nlead ? r : tail + (r - nlead);
+    const int key = r < nlead ? r0 + r : tail_beg + (r - nlead);
     const int rem = e % per_row;
     *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kTcKeys * 128) + key * 128 + (rem & 7) * 16) =
         make_uint4(0u, 0u, 0u, 0u);
@@ -279,7 +291,7 @@ __device__ __forceinline__ void widen_tile_fp8_d64(uint8_t* tile, int lane) {
 // ranked by the number of 128-key tiles their rows see (a chunk's last
 // pairs, and longer contexts, see more), ties by index, and the kv heads of a
 // unit are consecutive CTAs.  Every CTA ranks the units itself (at most
-// kLptUnits costs, in shared memory scratch that the K ring later reuses).
+// kLptUnits costs, in shared memory scratch that the K/V ring later reuses).
 // Otherwise, or with more than kLptUnits units (many waves, little tail), the
 // grid keeps its plain order (heaviest pair of each sequence first).
 // Measured on GB300, the 4 x 512-token chunks of the mixed 32 q / 8 kv head
@@ -332,7 +344,7 @@ __device__ __forceinline__ TcWork pick_work(const PrefillArgs& a, int toks, int3
     }
     if (rank == r) *pick = u;
   }
-  fence_proxy_async();   // the K ring's TMA writes later land on this scratch
+  fence_proxy_async();   // the ring's TMA writes later land on this scratch
   __syncthreads();
   const int u = *pick;
   return TcWork{a.seq_begin + u / a.num_mtiles, b % a.num_kv_heads, u % a.num_mtiles};
@@ -351,9 +363,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                                   // [tile][half][128 rows x 128 B]
-  uint8_t* sK = smem + kTcTiles * Lt::kQTile;           // [K stage][half][128 keys x 128 B]
-  uint8_t* sV = sK + kKStages * Lt::kTileBytes;         // [V stage][half][128 keys x 128 B]
-  TcShared* sh = reinterpret_cast<TcShared*>(sV + kVStages * Lt::kTileBytes);
+  uint8_t* sKV = smem + kTcTiles * Lt::kQTile;          // [slot][half][128 keys x 128 B]
+  TcShared* sh = reinterpret_cast<TcShared*>(sKV + kRing * Lt::kTileBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -367,7 +378,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int toks = kTcTiles * tile_toks;            // tokens per CTA
   int s, kvh, mtile;
   if constexpr (LPT) {
-    const TcWork w = pick_work(a, toks, reinterpret_cast<int32_t*>(sK));
+    const TcWork w = pick_work(a, toks, reinterpret_cast<int32_t*>(sKV));
     s = w.s;
     kvh = w.kvh;
     mtile = w.mtile;
@@ -463,15 +474,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(&sh->issued[t]), 1);
       mbar_init(smem_u32(&sh->drain[t]), 1);
     }
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(smem_u32(&sh->k_full[i]), 1);
-      mbar_init(smem_u32(&sh->k_empty[i]), issuers);
-      mbar_init(smem_u32(&sh->k_land[i]), 1);
-    }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(smem_u32(&sh->v_full[i]), 1);
-      mbar_init(smem_u32(&sh->v_empty[i]), issuers);
-      mbar_init(smem_u32(&sh->v_land[i]), 1);
+    for (int i = 0; i < kRing; ++i) {
+      // FP8 D = 128: both widening warps arrive (each widens half the rows)
+      mbar_init(smem_u32(&sh->kv_full[i]), (FP8 && D == 128) ? 2 : 1);
+      mbar_init(smem_u32(&sh->kv_empty[i]), issuers);
+      mbar_init(smem_u32(&sh->kv_land[i]), 1);
     }
     sh->abort = 0;
     fence_barrier_init();
@@ -505,11 +512,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // add per MMA on the issuing thread, whose instructions compete with
   // the softmax warps for the same issue slots.
   const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(sQ), 16, 1024);
-  const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(sK), 16, 1024);
-  const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(sV), Lt::kKvHalf, 1024);
+  const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(sKV), 16, 1024);
+  const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(sKV), Lt::kKvHalf, 1024);
   auto issue_s = [&](int t, int j) {
     const uint64_t da0 = dq0 + static_cast<uint64_t>((t * Lt::kQTile) >> 4);
-    const uint64_t db0 = dk0 + static_cast<uint64_t>(((j % kKStages) * Lt::kTileBytes) >> 4);
+    const uint64_t db0 =
+        dk0 + static_cast<uint64_t>((ring_slot(2 * j) * Lt::kTileBytes) >> 4);
     const uint32_t d = tmem + col_s(t);
     // K-step k: 16 bf16 = 32 B along the swizzled 128-B row, 64 columns
     // per half (16 KB apart for both operands)
@@ -525,7 +533,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::commit(smem_u32(&sh->s_full[t]));
   };
   auto issue_pv = [&](int t, int j) {
-    const uint64_t db0 = dv0 + static_cast<uint64_t>(((j % kVStages) * Lt::kTileBytes) >> 4);
+    const uint64_t db0 =
+        dv0 + static_cast<uint64_t>((ring_slot(2 * j + 1) * Lt::kTileBytes) >> 4);
     tc::mma_ts_x8(tmem + col_o(t), tmem + col_p(t), db0, idO, j > 0 ? 1u : 0u);
     tc::commit(smem_u32(&sh->pv_done[t]));
   };
@@ -535,10 +544,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
    set_max_regs_dec_other();
    if (warp == 8 || (!FP8 && warp == 10)) {
     // ------------------------------------------------------------ producers
-    // bf16: warp 8 streams the K tiles and warp 10 the V tiles, each through
-    // its own ring, so that neither waits behind the other's ring.  FP8:
-    // warp 8 streams both (K of tile it before V of tile it - 1); warps 10
-    // and 11 widen them.
+    // bf16: warp 8 streams the K tiles and warp 10 the V tiles into their
+    // ring slots, each waiting only for its own slots.  FP8: warp 8 streams
+    // both (K of tile it before V of tile it - 1); warps 10 and 11 widen
+    // them.
     const uint64_t keep = policy_evict_normal();   // K/V tiles are re-read by the
     const int32_t* bt = a.block_tables + static_cast<int64_t>(s) * a.bt_stride;  // other row tiles
     if (warp == 8 && lane == 0) {
@@ -594,121 +603,122 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     };
-    int g_prev = -1, g_cur = load_ids4(0), g_nxt = load_ids4(1);
+    int g_cur = load_ids4(0), g_nxt = load_ids4(1);
     // Test hook: the K producer withholds the first K tile (no copy, no
     // arrival), so that the waits for it run out.
     const bool withhold_k0 = a.debug_stall != 0;
-    // Before the CTA's shared memory is released, every copy a producer
-    // started must have landed: after its loop (normal or given up) it waits,
-    // with the full limit, for the last tile of each ring stage it filled
-    // (earlier ones were consumed before the stage was refilled).
-    auto drain = [&](int n_issued, int stages, bool is_v, bool land) {
-      for (int r = max(0, n_issued - stages); r < n_issued; ++r) {
-        if (!is_v && r == 0 && withhold_k0) continue;
-        const int st = r % stages;
-        const uint32_t bar = smem_u32(land ? (is_v ? &sh->v_land[st] : &sh->k_land[st])
-                                           : (is_v ? &sh->v_full[st] : &sh->k_full[st]));
-        if (lane == 0) (void)mbar_wait(bar, (r / stages) & 1);
+    // Before the CTA's shared memory is released every copy a producer
+    // started must have landed.  Only the last use of a slot can still be in
+    // flight: element e's slot is refilled by element e + kRing only after e
+    // has been read (so has landed).  Waits on a slot's barrier with e's
+    // parity are then exact (no later phase of that barrier exists).
+    // n_k / n_v: K / V tiles this warp issued (ring positions 0 .. n - 1),
+    // n_k_all / n_v_all: by either producer; `skip`: a ring element whose
+    // copy was already waited for (or never started).
+    auto drain = [&](int n_k, int n_v, int n_k_all, int n_v_all, bool land, int skip) {
+      for (int e = 0; e < 2 * max(n_k, n_v); ++e) {
+        const bool mine_k = !(e & 1) && (e >> 1) < n_k, mine_v = (e & 1) && (e >> 1) < n_v;
+        if (!(mine_k || mine_v) || e == skip) continue;
+        const int nx = e + kRing;   // the slot's next element: issued?
+        if ((nx & 1) ? (nx >> 1) < n_v_all : (nx >> 1) < n_k_all) continue;
+        const int st = ring_slot(e);
+        const uint32_t bar = smem_u32(land ? &sh->kv_land[st] : &sh->kv_full[st]);
+        if (lane == 0) (void)mbar_wait(bar, ring_phase(e));
       }
       __syncwarp();
     };
     if constexpr (!FP8) {
       const bool is_v = warp == 10;
-      const int stages = is_v ? kVStages : kKStages;
-      uint32_t land_phase = 0;   // parity of each stage's next v_land phase
-      int n_issued = 0, pending_land = -1;
+      uint32_t land_phase = 0;   // parity of each slot's next kv_land phase (V edges)
+      int n_issued = 0, pending_land = -1, pending_e = -1;
       for (int rel = 0; rel < n_rel; ++rel) {
         if (rel > 0 && (rel & 3) == 0) {
           g_cur = g_nxt;
           g_nxt = load_ids4((rel >> 2) + 1);
         }
-        const int st = rel % stages;
-        if (rel >= stages &&
-            !warp_wait(smem_u32(is_v ? &sh->v_empty[st] : &sh->k_empty[st]),
-                       ((rel / stages) - 1) & 1, abort, a.err, wlim))
+        const int e = 2 * rel + (is_v ? 1 : 0);
+        const int st = ring_slot(e);
+        if (e >= kRing && !warp_wait(smem_u32(&sh->kv_empty[st]), ring_phase(e - kRing), abort,
+                                     a.err, wlim))
           break;
         int lead, tail;
         const bool edge = is_v && v_edges(rel, lead, tail);
         if (!(!is_v && rel == 0 && withhold_k0))
-          issue_tile(j0 + rel, g_cur, rel & 3, is_v,
-                     smem_u32((is_v ? sV : sK) + st * Lt::kTileBytes),
-                     smem_u32(edge ? &sh->v_land[st] : is_v ? &sh->v_full[st] : &sh->k_full[st]));
+          issue_tile(j0 + rel, g_cur, rel & 3, is_v, smem_u32(sKV + st * Lt::kTileBytes),
+                     smem_u32(edge ? &sh->kv_land[st] : &sh->kv_full[st]));
         n_issued = rel + 1;
         if (lane == 0) TC_MARK((is_v ? 200 : 100) + (rel & 63));
         if (edge) {   // landed, edge rows zeroed, then full
           pending_land = st;
-          if (!warp_wait(smem_u32(&sh->v_land[st]), (land_phase >> st) & 1u, abort, a.err, wlim))
+          pending_e = e;
+          if (!warp_wait(smem_u32(&sh->kv_land[st]), (land_phase >> st) & 1u, abort, a.err, wlim))
             break;
           pending_land = -1;
           land_phase ^= 1u << st;
-          zero_v_rows<D>(sV + st * Lt::kTileBytes, lead, tail, lane);
+          zero_v_rows<D>(sKV + st * Lt::kTileBytes, lead, tail, 0, kTcKeys, lane);
           fence_proxy_async();   // generic writes, then the tensor core reads
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sh->v_full[st]));
+          if (lane == 0) mbar_arrive(smem_u32(&sh->kv_full[st]));
         }
       }
-      // An edge tile whose landing wait gave up is still in flight on v_land;
-      // the other tiles' copies complete on their full barriers.
+      // An edge tile whose landing wait gave up is still in flight on
+      // kv_land; the other tiles' copies complete on kv_full.
       if (pending_land >= 0 && lane == 0)
-        (void)mbar_wait(smem_u32(&sh->v_land[pending_land]), (land_phase >> pending_land) & 1u);
-      drain(pending_land >= 0 ? n_issued - 1 : n_issued, stages, is_v, false);
+        (void)mbar_wait(smem_u32(&sh->kv_land[pending_land]), (land_phase >> pending_land) & 1u);
+      if (lane == 0) sh->n_issued[is_v ? 1 : 0] = n_issued;
+      named_barrier(3, 64);   // warps 8 and 10: both counts final
+      drain(is_v ? 0 : n_issued, is_v ? n_issued : 0, sh->n_issued[0], sh->n_issued[1], false,
+            pending_land >= 0 ? pending_e : (withhold_k0 && !is_v ? 0 : -1));
     } else {
+      // one warp, ring elements in order: K(0), V(0), K(1), ...
       int k_issued = 0, v_issued = 0;
-      for (int rel = 0; rel <= n_rel; ++rel) {
-        if (rel > 0 && (rel & 3) == 0) {
-          g_prev = g_cur;
+      for (int e = 0; e < 2 * n_rel; ++e) {
+        const int rel = e >> 1;
+        const bool is_v = (e & 1) != 0;
+        if (!is_v && rel > 0 && (rel & 3) == 0) {
           g_cur = g_nxt;
           g_nxt = load_ids4((rel >> 2) + 1);
         }
-        if (rel < n_rel) {
-          const int st = rel % kKStages;
-          if (rel >= kKStages &&
-              !warp_wait(smem_u32(&sh->k_empty[st]), ((rel / kKStages) - 1) & 1, abort, a.err, wlim))
-            break;
-          // (the codes land on k_land; warp 10 widens them, then k_full)
-          if (!(rel == 0 && withhold_k0))
-            issue_tile(j0 + rel, g_cur, rel & 3, false, smem_u32(sK + st * Lt::kTileBytes),
-                       smem_u32(&sh->k_land[st]));
-          k_issued = rel + 1;
-          if (lane == 0) TC_MARK(100 + (rel & 63));
-        }
-        if (rel >= 1) {
-          const int rv = rel - 1;   // ring position of the V tile
-          const int st = rv % kVStages;
-          if (rv >= kVStages &&
-              !warp_wait(smem_u32(&sh->v_empty[st]), ((rv / kVStages) - 1) & 1, abort, a.err, wlim))
-            break;
-          issue_tile(j0 + rv, (rv >> 2) == (rel >> 2) ? g_cur : g_prev, rv & 3, true,
-                     smem_u32(sV + st * Lt::kTileBytes), smem_u32(&sh->v_land[st]));
-          v_issued = rv + 1;
-          if (lane == 0) TC_MARK(200 + (rv & 63));
-        }
+        const int st = ring_slot(e);
+        if (e >= kRing && !warp_wait(smem_u32(&sh->kv_empty[st]), ring_phase(e - kRing), abort,
+                                     a.err, wlim))
+          break;
+        // (the codes land on kv_land; warps 10 and 11 widen them, then kv_full)
+        if (!(e == 0 && withhold_k0))
+          issue_tile(j0 + rel, g_cur, rel & 3, is_v, smem_u32(sKV + st * Lt::kTileBytes),
+                     smem_u32(&sh->kv_land[st]));
+        (is_v ? v_issued : k_issued) = rel + 1;
+        if (lane == 0) TC_MARK((is_v ? 200 : 100) + (rel & 63));
       }
-      drain(k_issued, kKStages, false, true);
-      drain(v_issued, kVStages, true, true);
+      drain(k_issued, v_issued, k_issued, v_issued, true, withhold_k0 ? 0 : -1);
     }
     if (warp == 8 && lane == 0) (void)mbar_wait(q_full, 0);   // the query tiles too
     __syncwarp();
-   } else if (FP8 && warp >= 10) {
+   } else if (FP8 && (warp == 10 || (D == 128 && warp == 11))) {
     // ------------------------------------------------- widen e4m3 tiles (FP8)
-    const bool is_v = warp == 11;
-    for (int i = 0; i < n_rel; ++i) {
-      const int st = is_v ? i % kVStages : i % kKStages;
-      const int ph = is_v ? (i / kVStages) & 1 : (i / kKStages) & 1;
-      if (!warp_wait(smem_u32(is_v ? &sh->v_land[st] : &sh->k_land[st]), ph, abort, a.err, wlim))
-        break;
+    // Ring elements in order, so that each wait on a slot's kv_land is for
+    // the phase after the last one this warp saw there.  D = 128: warp 10
+    // widens rows 0-63 and warp 11 rows 64-127 of every tile.  D = 64: the
+    // in-place widening overwrites later rows' codes with earlier rows' fp16
+    // (it runs from the last rows to the first), so warp 10 takes whole tiles.
+    const int r0 = D == 128 ? 64 * (warp - 10) : 0;
+    const int r1 = D == 128 ? r0 + 64 : kTcKeys;
+    for (int e = 0; e < 2 * n_rel; ++e) {
+      const int st = ring_slot(e);
+      if (!warp_wait(smem_u32(&sh->kv_land[st]), ring_phase(e), abort, a.err, wlim)) break;
+      uint8_t* tile = sKV + st * Lt::kTileBytes;
       if constexpr (D == 128)
-        widen_tile_fp8(is_v ? sV + st * Lt::kTileBytes : sK + st * Lt::kTileBytes, lane);
+        widen_tile_fp8(tile, lane, r0 / 16, r1 / 16);
       else
-        widen_tile_fp8_d64(is_v ? sV + st * Lt::kTileBytes : sK + st * Lt::kTileBytes, lane);
+        widen_tile_fp8_d64(tile, lane);
       int lead, tail;
-      if (is_v && v_edges(i, lead, tail)) {
+      if ((e & 1) && v_edges(e >> 1, lead, tail)) {
         __syncwarp();
-        zero_v_rows<D>(sV + st * Lt::kTileBytes, lead, tail, lane);
+        zero_v_rows<D>(tile, lead, tail, r0, r1, lane);
       }
       fence_proxy_async();   // generic writes, then the tensor core reads
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(is_v ? &sh->v_full[st] : &sh->k_full[st]));
+      if (lane == 0) mbar_arrive(smem_u32(&sh->kv_full[st]));
     }
    }
   } else {
@@ -795,12 +805,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t other_issued = smem_u32(&sh->issued[t ^ 1]);
     if (issuer) {
       if (wait_or_abort(q_ready, 0, abort, a.err, wlim) &&
-          wait_or_abort(smem_u32(&sh->k_full[0]), 0, abort, a.err, wlim) &&
+          wait_or_abort(smem_u32(&sh->kv_full[ring_slot(0)]), ring_phase(0), abort, a.err, wlim) &&
           (t == 0 || wait_or_abort(other_issued, 0, abort, a.err, wlim))) {
         tc::fence_after_sync();
         TC_MARK(300 + 64 * t);
         issue_s(t, 0);
-        tc::commit(smem_u32(&sh->k_empty[0]));
+        tc::commit(smem_u32(&sh->kv_empty[ring_slot(0)]));
         mbar_arrive(my_issued);
       }
     }
@@ -899,20 +909,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // this tile's group j: after the other tile's group j - 1 (tile 0)
         // or group j (tile 1), i.e. the other barrier's phase j or j + 1
         if (wait_or_abort(b_pfull, j & 1, abort, a.err, wlim) &&
-            wait_or_abort(smem_u32(&sh->v_full[j % kVStages]), (j / kVStages) & 1, abort,
+            wait_or_abort(smem_u32(&sh->kv_full[ring_slot(2 * j + 1)]), ring_phase(2 * j + 1), abort,
                           a.err, wlim) &&
             (!paired || wait_or_abort(other_issued, (j + t) & 1, abort, a.err, wlim))) {
           tc::fence_after_sync();
           TC_MARK(500 + 64 * t + (j & 63));
           issue_pv(t, j);
-          tc::commit(smem_u32(&sh->v_empty[j % kVStages]));
+          tc::commit(smem_u32(&sh->kv_empty[ring_slot(2 * j + 1)]));
           const int jn = j + 1;
-          if (jn < n_rel && wait_or_abort(smem_u32(&sh->k_full[jn % kKStages]),
-                                          (jn / kKStages) & 1, abort, a.err, wlim)) {
+          if (jn < n_rel && wait_or_abort(smem_u32(&sh->kv_full[ring_slot(2 * jn)]),
+                                          ring_phase(2 * jn), abort, a.err, wlim)) {
             tc::fence_after_sync();
             TC_MARK(300 + 64 * t + (jn & 63));
             issue_s(t, jn);
-            tc::commit(smem_u32(&sh->k_empty[jn % kKStages]));
+            tc::commit(smem_u32(&sh->kv_empty[ring_slot(2 * jn)]));
           }
           mbar_arrive(my_issued);
         }
