@@ -820,6 +820,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!warp_wait(b_sfull, j & 1, abort, a.err, wlim)) { done = false; break; }
       tc::fence_after_sync();
       if (quarter == 0 && lane == 0) TC_MARK(700 + 64 * t + (j & 63));
+      if (t == 0 && quarter > 0 && lane == 0 && j < 32) TC_MARK(1030 + 32 * (quarter - 1) + j);
       float x[kTcKeys];
 #pragma unroll
       for (int c0 = 0; c0 < kTcKeys; c0 += 32) {
@@ -904,14 +905,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pfull);
       if (quarter == 0 && lane == 0) TC_MARK(900 + 64 * t + (j & 63));
+      if (t == 0 && lane == 0) TC_MARK(1700 + 64 * quarter + (j & 63));
       if (issuer) {
         // (a failed wait leaves the other warps to give up on s_full)
         // this tile's group j: after the other tile's group j - 1 (tile 0)
         // or group j (tile 1), i.e. the other barrier's phase j or j + 1
-        if (wait_or_abort(b_pfull, j & 1, abort, a.err, wlim) &&
-            wait_or_abort(smem_u32(&sh->kv_full[ring_slot(2 * j + 1)]), ring_phase(2 * j + 1), abort,
-                          a.err, wlim) &&
-            (!paired || wait_or_abort(other_issued, (j + t) & 1, abort, a.err, wlim))) {
+        bool go = wait_or_abort(b_pfull, j & 1, abort, a.err, wlim);
+        if (go) TC_MARK(1528 + 64 * t + (j & 63));
+        go = go && wait_or_abort(smem_u32(&sh->kv_full[ring_slot(2 * j + 1)]),
+                                 ring_phase(2 * j + 1), abort, a.err, wlim);
+        if (go) TC_MARK(1400 + 64 * t + (j & 63));
+        if (go && (!paired || wait_or_abort(other_issued, (j + t) & 1, abort, a.err, wlim))) {
           tc::fence_after_sync();
           TC_MARK(500 + 64 * t + (j & 63));
           issue_pv(t, j);
