@@ -145,6 +145,16 @@ def test_fp8_prefill_edge_chunks(hq, hkv, d):
     assert max_err(out, exp) <= TOL_FP8
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_prefill_full_tiles_one_head_per_group(d):
+    """G = 1 with chunks of 128 tokens or more: full query tiles (TMA-stored
+    rows) and partial ones, over widened e4m3 tiles."""
+    wl = W.make_workload([128, 129, 256, 300, 1], [128, 500, 256, 700, 50], num_q_heads=8,
+                         num_kv_heads=8, head_size=d, seed=9 + d)
+    out, exp, _, _ = _run(wl)
+    assert max_err(out, exp) <= TOL_FP8
+
+
 def test_fp8_mixed_batch_with_prefix_sharing():
     out, exp, _, _ = _run(W.workload(4, small=True))
     assert max_err(out, exp) <= TOL_FP8

@@ -116,6 +116,21 @@ def test_prefill_edge_chunks(hq, hkv, d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_prefill_full_tiles_one_head_per_group(d):
+    """G = 1: a query tile is 128 tokens, so only chunks of 128 tokens or more
+    have full tiles, whose rows leave through shared memory and a TMA store
+    (a box of one head x 128 tokens).  The 129- and 300-token chunks end in a
+    partial tile written row by row; the 128-token chunk has no second tile."""
+    q_lens = [128, 129, 256, 300, 1]
+    ctx = [128, 500, 256, 700, 50]
+    wl = W.make_workload(q_lens, ctx, num_q_heads=8, num_kv_heads=8, head_size=d,
+                         dtype=torch.bfloat16, seed=5 + d)
+    exp, _, _, _ = oracle_step(wl)
+    _, out = _run(wl)
+    assert max_err(out, exp) <= 2e-2
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_f32_decode_and_prefill(d):
     wl = W.make_workload([1, 3, 17, 1], [17, 40, 70, 100], num_q_heads=4, num_kv_heads=2,
                          head_size=d, dtype=torch.float32, seed=d)
